@@ -1,0 +1,357 @@
+// The C ABI declared in include/prox.h: argument validation, buffer carving and the order
+// of launches. Every step of the computation runs in the kernels; this file only decides
+// what to launch, on which stream, with which pointers.
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "prox_kernels.cuh"
+
+using namespace prox;
+
+namespace {
+
+constexpr int kMaxDModel = 16384;
+constexpr int kMaxDff = 57344;   // the top-k block keeps one salience row in shared memory
+
+bool shape_ok(int d, int F) {
+    return d >= 128 && d <= kMaxDModel && d % 128 == 0 && F >= 32 && F <= kMaxDff && F % 32 == 0;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool sparsity_ok(double s) { return s >= 0.0 && s < 1.0; }
+
+int k_rule(double s, int n) {
+    const double v = std::floor((1.0 - s) * static_cast<double>(n) + 0.5);
+    long long k = static_cast<long long>(v);
+    if (k < 1) k = 1;
+    if (k > n) k = n;
+    return static_cast<int>(k);
+}
+
+int device_sms() {
+    static std::mutex mu;
+    static int cache[128] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return -1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+        cache[dev] = sms;
+    }
+    return cache[dev];
+}
+
+// Checks a packed descriptor. Returns PROX_OK or an error code.
+int check_packed(const prox_packed* w) {
+    if (!w || !w->base) return PROX_ERR_INVALID_ARG;
+    if (w->group != PROX_GROUP || !shape_ok(w->d_model, w->d_ff)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(w->base, kAlign)) return PROX_ERR_WORKSPACE;
+    if (w->bytes < packed_layout(w->d_model, w->d_ff).total) return PROX_ERR_WORKSPACE;
+    return PROX_OK;
+}
+
+int check_ws(void* ws, size_t ws_bytes, int d, int F, int B, int sms, WsLayout& W) {
+    if (!ws) return PROX_ERR_INVALID_ARG;
+    if (!aligned(ws, kAlign)) return PROX_ERR_WORKSPACE;
+    W = ws_layout(d, F, B, sms);
+    if (ws_bytes < W.total) return PROX_ERR_WORKSPACE;
+    return PROX_OK;
+}
+
+#define PROX_TRY(expr)                 \
+    do {                               \
+        const int rc_ = (expr);        \
+        if (rc_ != PROX_OK) return rc_; \
+    } while (0)
+
+// Stage 2 for one tile of tokens: a single token uses its mask directly, several tokens
+// share the union of their masks (one read of each selected row per tile).
+int run_stage2_tile(const prox_packed* w, const PackedLayout& L, const float* xt, int nb,
+                    const int32_t* idx_tile, int k, bool dense, float* yt, uint8_t* ws,
+                    const WsLayout& W, int sms, cudaStream_t s) {
+    const int d = w->d_model, F = w->d_ff;
+    const uint8_t* packed = static_cast<const uint8_t*>(w->base);
+    if (dense)
+        return launch_stage2(packed, L, d, F, xt, nb, nullptr, nullptr, nullptr, F, yt, ws, W,
+                             sms, s);
+    if (nb == 1)
+        return launch_stage2(packed, L, d, F, xt, nb, idx_tile, nullptr, nullptr, k, yt, ws, W,
+                             sms, s);
+    Control* ctrl = reinterpret_cast<Control*>(ws + W.control);
+    int32_t* ulist = reinterpret_cast<int32_t*>(ws + W.ulist);
+    uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
+    PROX_TRY(launch_union(idx_tile, nb, k, F, ulist, ubits, &ctrl->union_count, &ctrl->status, s));
+    return launch_stage2(packed, L, d, F, xt, nb, ulist, ubits, &ctrl->union_count, 0, yt, ws, W,
+                         sms, s);
+}
+
+struct Debug {
+    int8_t* qx = nullptr;
+    float* sx = nullptr;
+    int32_t* acc_gate = nullptr;
+    int32_t* acc_up = nullptr;
+    float* salience = nullptr;
+};
+
+// The whole path over all tiles. y == nullptr stops after the mask.
+int run_path(const prox_packed* w, const float* x, int B, double sparsity, double in_sparsity,
+             float* y, int32_t* idx_out, uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s,
+             const Debug* dbg) {
+    const int d = w->d_model, F = w->d_ff, G = d / 128;
+    const PackedLayout L = packed_layout(d, F);
+    const uint8_t* packed = static_cast<const uint8_t*>(w->base);
+    const int k = k_rule(sparsity, F);
+    const int k_in = k_rule(in_sparsity, d);
+    const bool all_channels = (k == F) && !dbg;
+    int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + W.idx);
+    float* sigma = (dbg && dbg->salience) ? dbg->salience : reinterpret_cast<float*>(ws + W.sigma);
+    for (int t0 = 0; t0 < B; t0 += W.TB) {
+        const int nb = B - t0 < W.TB ? B - t0 : W.TB;
+        const float* xt = x + static_cast<size_t>(t0) * d;
+        int32_t* idx_t = idx + static_cast<size_t>(t0) * k;
+        if (all_channels) {
+            // sparsity 0: every channel is kept, the ranking cannot change the result
+            if (idx_out) PROX_TRY(launch_iota(idx_t, F, nb, s));
+            if (y)
+                PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, true,
+                                         y + static_cast<size_t>(t0) * d, ws, W, sms, s));
+            continue;
+        }
+        PROX_TRY(launch_input_quant(xt, d, nb, k_in, ws, W,
+                                    dbg && dbg->qx ? dbg->qx + static_cast<size_t>(t0) * d : nullptr,
+                                    dbg && dbg->sx ? dbg->sx + static_cast<size_t>(t0) * G : nullptr, s));
+        PROX_TRY(launch_stage1(packed, L, d, F, nb, k_in, ws, W, sigma + static_cast<size_t>(t0) * F,
+                               dbg && dbg->acc_gate ? dbg->acc_gate + static_cast<size_t>(t0) * G * F : nullptr,
+                               dbg && dbg->acc_up ? dbg->acc_up + static_cast<size_t>(t0) * G * F : nullptr,
+                               sms, s));
+        if (dbg) continue;
+        PROX_TRY(launch_topk(sigma + static_cast<size_t>(t0) * F, F, nb, k, idx_t, s));
+        if (y)
+            PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, false, y + static_cast<size_t>(t0) * d,
+                                     ws, W, sms, s));
+    }
+    return PROX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t prox_packed_bytes(int d_model, int d_ff, int group) {
+    if (group != PROX_GROUP || !shape_ok(d_model, d_ff)) return 0;
+    return packed_layout(d_model, d_ff).total;
+}
+
+size_t prox_workspace_bytes(int d_model, int d_ff, int batch) {
+    if (!shape_ok(d_model, d_ff) || batch < 1 || batch > PROX_MAX_BATCH) return 0;
+    const int sms = device_sms();
+    if (sms <= 0) return 0;
+    return ws_layout(d_model, d_ff, batch, sms).total;
+}
+
+int prox_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws) return PROX_ERR_INVALID_ARG;
+    if (!aligned(ws, kAlign)) return PROX_ERR_WORKSPACE;
+    const size_t need = ws_control_bytes((kMaxDff + 127) / 128);
+    if (ws_bytes < align_up(sizeof(Control))) return PROX_ERR_WORKSPACE;
+    const size_t n = ws_bytes < need ? ws_bytes : need;
+    return cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PROX_OK
+                                                                                       : PROX_ERR_CUDA;
+}
+
+int prox_k_for(double sparsity, int n) {
+    if (!sparsity_ok(sparsity) || n < 1) return -1;
+    return k_rule(sparsity, n);
+}
+
+int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                      int d_model, int d_ff, int group, void* packed_dev, size_t packed_bytes,
+                      void* stream, prox_packed* out) {
+    if (!w_gate || !w_up || !w_down || !packed_dev || !out) return PROX_ERR_INVALID_ARG;
+    if (group != PROX_GROUP || !shape_ok(d_model, d_ff)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(packed_dev, kAlign)) return PROX_ERR_WORKSPACE;
+    const PackedLayout L = packed_layout(d_model, d_ff);
+    if (packed_bytes < L.total) return PROX_ERR_WORKSPACE;
+    PROX_TRY(launch_pack(w_gate, w_up, w_down, d_model, d_ff, L, static_cast<uint8_t*>(packed_dev),
+                         static_cast<cudaStream_t>(stream)));
+    out->d_model = d_model;
+    out->d_ff = d_ff;
+    out->group = group;
+    out->reserved = 0;
+    out->base = packed_dev;
+    out->bytes = packed_bytes;
+    return PROX_OK;
+}
+
+int prox_build_mask(const prox_packed* w, const float* x, int batch, double sparsity,
+                    double input_sparsity, int32_t* idx_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !idx_out || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    return run_path(w, x, batch, sparsity, input_sparsity, nullptr, idx_out,
+                    static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx, int k,
+                    float* y, void* ws, size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !idx || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (k < 1 || k > w->d_ff) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    const PackedLayout L = packed_layout(w->d_model, w->d_ff);
+    const int d = w->d_model;
+    for (int t0 = 0; t0 < batch; t0 += W.TB) {
+        const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
+        PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb,
+                                 idx + static_cast<size_t>(t0) * k, k, false,
+                                 y + static_cast<size_t>(t0) * d, static_cast<uint8_t*>(ws), W, sms,
+                                 static_cast<cudaStream_t>(stream)));
+    }
+    return PROX_OK;
+}
+
+int prox_ffn_forward(const prox_packed* w, const float* x, int batch, double sparsity,
+                     double input_sparsity, float* y, int32_t* idx_out, void* ws, size_t ws_bytes,
+                     void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    return run_path(w, x, batch, sparsity, input_sparsity, y, idx_out, static_cast<uint8_t*>(ws), W,
+                    sms, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch, double sparsity,
+                          double input_sparsity, float* y_host, void* ws, size_t ws_bytes,
+                          void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x_host || !y_host || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    float* xd = reinterpret_cast<float*>(wsb + W.xbuf);
+    float* yd = reinterpret_cast<float*>(wsb + W.ybuf);
+    const size_t bytes = static_cast<size_t>(batch) * w->d_model * sizeof(float);
+    if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return PROX_ERR_CUDA;
+    PROX_TRY(run_path(w, xd, batch, sparsity, input_sparsity, yd, nullptr, wsb, W, sms, s, nullptr));
+    if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PROX_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+}
+
+int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, void* ws,
+                   size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    const PackedLayout L = packed_layout(w->d_model, w->d_ff);
+    const int d = w->d_model;
+    for (int t0 = 0; t0 < batch; t0 += W.TB) {
+        const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
+        PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb, nullptr, w->d_ff, true,
+                                 y + static_cast<size_t>(t0) * d, static_cast<uint8_t*>(ws), W, sms,
+                                 static_cast<cudaStream_t>(stream)));
+    }
+    return PROX_OK;
+}
+
+int prox_rmsnorm(const float* y, float* x_out, int batch, int d_model, float eps, void* stream) {
+    if (!y || !x_out || batch < 1 || d_model < 1 || !(eps >= 0.f)) return PROX_ERR_INVALID_ARG;
+    return launch_rmsnorm(y, x_out, batch, d_model, eps, static_cast<cudaStream_t>(stream));
+}
+
+int prox_get_status(void* ws, void* stream) {
+    if (!ws) return PROX_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    Control* ctrl = static_cast<Control*>(ws);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PROX_ERR_CUDA;
+    if (cudaMemcpyAsync(&host, &ctrl->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PROX_ERR_CUDA;
+    if (cudaMemsetAsync(&ctrl->status, 0, sizeof(int), s) != cudaSuccess) return PROX_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PROX_ERR_CUDA;
+    return host;
+}
+
+const char* prox_error_string(int code) {
+    switch (code) {
+        case PROX_OK: return "ok";
+        case PROX_ERR_INVALID_ARG: return "invalid argument";
+        case PROX_ERR_WORKSPACE: return "workspace or packed buffer too small or misaligned";
+        case PROX_ERR_CUDA: return "CUDA runtime error";
+        case PROX_ERR_TIMEOUT: return "device wait timed out";
+        case PROX_ERR_BOUNDS: return "device index out of range";
+        case PROX_ERR_UNSUPPORTED: return "unsupported";
+        default: return "unknown error";
+    }
+}
+
+int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double input_sparsity,
+                      int8_t* qx_out, float* sx_out, int32_t* acc_gate, int32_t* acc_up,
+                      float* salience, void* ws, size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || batch < 1 || batch > PROX_MAX_BATCH || !sparsity_ok(input_sparsity))
+        return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t acc_bytes = static_cast<size_t>(batch) * (w->d_model / 128) * w->d_ff * 4;
+    if (acc_gate && cudaMemsetAsync(acc_gate, 0, acc_bytes, s) != cudaSuccess) return PROX_ERR_CUDA;
+    if (acc_up && cudaMemsetAsync(acc_up, 0, acc_bytes, s) != cudaSuccess) return PROX_ERR_CUDA;
+    Debug dbg;
+    dbg.qx = qx_out;
+    dbg.sx = sx_out;
+    dbg.acc_gate = acc_gate;
+    dbg.acc_up = acc_up;
+    dbg.salience = salience;
+    return run_path(w, x, batch, 0.5, input_sparsity, nullptr, nullptr, static_cast<uint8_t*>(ws), W,
+                    sms, s, &dbg);
+}
+
+int prox_debug_union(const int32_t* idx, int batch, int k, int d_ff, int32_t* union_out,
+                     uint32_t* bits_out, int32_t* count_out, void* ws, size_t ws_bytes,
+                     void* stream) {
+    if (!idx || !union_out || !bits_out || !count_out || !ws) return PROX_ERR_INVALID_ARG;
+    if (batch < 1 || batch > 32 || k < 1 || d_ff < 1 || d_ff > kMaxDff || k > d_ff)
+        return PROX_ERR_INVALID_ARG;
+    if (ws_bytes < align_up(sizeof(Control))) return PROX_ERR_WORKSPACE;
+    Control* ctrl = static_cast<Control*>(ws);
+    return launch_union(idx, batch, k, d_ff, union_out, bits_out, count_out, &ctrl->status,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int prox_debug_wait_timeout(void* ws, size_t ws_bytes, long long spin_cycles, void* stream) {
+    if (!ws || spin_cycles < 0) return PROX_ERR_INVALID_ARG;
+    if (ws_bytes < align_up(sizeof(Control))) return PROX_ERR_WORKSPACE;
+    Control* ctrl = static_cast<Control*>(ws);
+    return launch_wait_probe(&ctrl->status, spin_cycles, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

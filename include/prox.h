@@ -1,0 +1,188 @@
+/*
+ * prox.h -- C ABI of the B300 (sm_103a) Prox sparse SwiGLU FFN decode path.
+ *
+ * The method: "Prox: Training-Free FFN Activation Sparsity via Approximate
+ * Intermediate-Channel Salience in LLMs". Stage 1 applies input sparsity to the FFN input
+ * x and runs INT4 proxies of W_gate and W_up to rank the intermediate channels by the
+ * magnitude of s~ = u~ (.) h~, giving one shared channel mask. Stage 2 computes only the
+ * masked channels exactly from the bf16 weights and runs the down projection over the same
+ * channels (technical summary, "Methodology: The Prox Framework"; the authors' abstract).
+ *
+ * Conventions for every call below.
+ *  - Ownership: every pointer is caller-owned memory; "device" pointers are CUDA device
+ *    memory of the current device. The library allocates nothing and frees nothing.
+ *  - Asynchrony: calls enqueue kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return at once. Only prox_get_status and prox_ffn_forward_host wait.
+ *  - Validation happens on the host before any launch. On a returned error nothing was
+ *    launched and no output was written.
+ *  - Errors: PROX_OK (0) or a negative PROX_ERR_* code. Device-side faults the kernels
+ *    detect themselves (a bounded wait that ran out, an index out of range) are recorded in
+ *    a status word inside the workspace and reported by prox_get_status.
+ *  - Layouts are row-major. bf16 is passed as uint16_t bit patterns.
+ *  - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff a multiple of 32 in
+ *    [32, 65536]; batch in [1, PROX_MAX_BATCH]. Inputs must be finite.
+ *  - Sparsities are fractions in [0, 1). The kept counts are
+ *        k    = clamp(floor((1 - sparsity) * d_ff + 0.5), 1, d_ff)
+ *        k_in = clamp(floor((1 - input_sparsity) * d_model + 0.5), 1, d_model)
+ *    computed in IEEE double (see prox_k_for). The pages ask for at least 30% of the inputs
+ *    to be kept (technical summary, "Sparsity Allocation", Stage 1 constraint); this is
+ *    documented, not enforced.
+ *  - A workspace must be initialised once with prox_workspace_init before its first use;
+ *    calls that overlap in time (different streams) need different workspaces.
+ */
+#ifndef PROX_H_
+#define PROX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PROX_OK               0
+#define PROX_ERR_INVALID_ARG (-1)  /* null pointer, bad shape, sparsity outside [0,1)      */
+#define PROX_ERR_WORKSPACE   (-2)  /* workspace or packed buffer too small or misaligned   */
+#define PROX_ERR_CUDA        (-3)  /* a CUDA runtime call or launch failed                 */
+#define PROX_ERR_TIMEOUT     (-4)  /* device status: a bounded wait ran out                */
+#define PROX_ERR_BOUNDS      (-5)  /* device status: an index was out of range             */
+#define PROX_ERR_UNSUPPORTED (-6)  /* valid request this build does not implement          */
+
+#define PROX_GROUP      128        /* proxy quantization group along d_model               */
+#define PROX_MAX_BATCH  16         /* tokens per call                                      */
+#define PROX_ALIGN      256        /* required alignment of packed and workspace buffers   */
+
+/* Descriptor of one packed layer. A plain view of caller-owned device memory that
+ * prox_pack_weights fills; copy it freely. Field meaning:
+ *   d_model, d_ff, group  the layer shape and the proxy group (128);
+ *   base, bytes           the packed device buffer (PROX_ALIGN-aligned) and its size.
+ * Packed layout inside base (offsets are multiples of PROX_ALIGN, in this order):
+ *   codes  [d_model][d_ff] uint8: byte (i, j) holds the INT4 proxy codes of input i for
+ *          channel j, W_gate in the low nibble and W_up in the high nibble, each stored
+ *          as q + 8 with q in [-7, 7] (input-major, so a kept input is one row);
+ *   scales [d_model/128][d_ff] uint32: the fp16 group scales, W_gate's in the low half and
+ *          W_up's in the high half;
+ *   rows   [d_ff][3][d_model] bf16: for channel j the rows W_gate[j,:], W_up[j,:] and
+ *          W_down[:,j] one after another (channel-major, one contiguous run per channel). */
+typedef struct prox_packed {
+    int32_t d_model;
+    int32_t d_ff;
+    int32_t group;
+    int32_t reserved;
+    void*   base;
+    size_t  bytes;
+} prox_packed;
+
+/* Bytes prox_pack_weights needs for one layer; 0 if the shape is invalid. */
+size_t prox_packed_bytes(int d_model, int d_ff, int group);
+
+/* Workspace bytes a call on this layer shape and batch needs on the CURRENT device (it
+ * depends on the device's SM count); 0 if the shape is invalid. One workspace serves every
+ * call on shapes no larger than the ones it was sized for. */
+size_t prox_workspace_bytes(int d_model, int d_ff, int batch);
+
+/* Clears the workspace's status word and its self-resetting counters. Call once after
+ * allocating a workspace, and again after prox_get_status reported a device error. */
+int prox_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* The kept-count rule above: clamp(floor((1 - sparsity) * n + 0.5), 1, n); -1 if the
+ * sparsity is outside [0, 1) or n < 1. */
+int prox_k_for(double sparsity, int n);
+
+/* Builds the Stage-1 proxies and the Stage-2 channel-major rows of one layer
+ * (technical summary, Stage 1 "Input Sparsity & Quantization": INT4 proxy weights for the
+ * up and gate projections; Stage 2 "Exact Projections": the original bf16 weights).
+ *   w_gate [d_ff][d_model], w_up [d_ff][d_model], w_down [d_model][d_ff]: device bf16 in
+ *          nn.Linear layout; read only, not needed after the call's kernels finish.
+ *   group  must be 128.
+ *   packed_dev / packed_bytes: device buffer of at least prox_packed_bytes() bytes,
+ *          PROX_ALIGN-aligned; written by the kernels.
+ *   out    host descriptor, filled on success.
+ * Proxy rule per channel j and group g of 128 inputs: a = max |w|,
+ * sw = fp16(fp32(a) / 7), q = clamp(rint(fp32(w) / fp32(sw)), -7, 7), q = 0 if sw == 0. */
+int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                      int d_model, int d_ff, int group,
+                      void* packed_dev, size_t packed_bytes, void* stream, prox_packed* out);
+
+/* Stage 1 alone: input sparsity, INT4 proxy projections, salience |SiLU(g~) * u~| and the
+ * top-k channel mask (technical summary, Stage 1 "Proxy Activation" and "Mask
+ * Generation"; abstract: the mask comes from the magnitude ranking of the entries).
+ *   x       [batch][d_model] fp32, device.
+ *   idx_out [batch][k] int32, device: per token the k selected channels in ascending order;
+ *           equal salience goes to the lower channel index.
+ *   ws      device workspace of at least prox_workspace_bytes(d_model, d_ff, batch). */
+int prox_build_mask(const prox_packed* w, const float* x, int batch,
+                    double sparsity, double input_sparsity,
+                    int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage 2 alone, for a given mask (technical summary, Stage 2 "Exact Projections" and
+ * "Final Output"): for each token b, y_b = sum over j in idx[b] of
+ * SiLU(W_gate[j,:] . x_b) * (W_up[j,:] . x_b) * W_down[:, j], with fp32 activations,
+ * bf16 weights and fp32 accumulation; the cross-block sum runs in a fixed order, so the
+ * result is bit-reproducible on a given device.
+ *   x   [batch][d_model] fp32 device;  idx [batch][k] int32 device, each row strictly
+ *   ascending in [0, d_ff);  y [batch][d_model] fp32 device (written). 1 <= k <= d_ff. */
+int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx,
+                    int k, float* y, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole path: Stage 1 mask, then Stage 2 over it. At sparsity 0 every channel is kept
+ * and Stage 1 is skipped (the result is the dense FFN).
+ *   y       [batch][d_model] fp32 device (written).
+ *   idx_out [batch][k] int32 device, or NULL when the mask is not wanted. */
+int prox_ffn_forward(const prox_packed* w, const float* x, int batch,
+                     double sparsity, double input_sparsity,
+                     float* y, int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/* prox_ffn_forward with HOST input and output: copies x_host (batch x d_model fp32) to the
+ * workspace, runs the path, copies y back to y_host, and waits for the stream. Pinned host
+ * buffers make the copies asynchronous with respect to other streams. */
+int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch,
+                          double sparsity, double input_sparsity,
+                          float* y_host, void* ws, size_t ws_bytes, void* stream);
+
+/* Dense SwiGLU FFN over every channel with the same kernel and weights (the baseline a
+ * sparse call is compared with; technical summary, "Problem Statement"). */
+int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Unit-gain RMSNorm between stacked layers: x_out = y / sqrt(mean(y^2) + eps), per row.
+ * y and x_out are [batch][d_model] fp32 device and may alias. */
+int prox_rmsnorm(const float* y, float* x_out, int batch, int d_model, float eps,
+                 void* stream);
+
+/* Waits for `stream`, then returns and clears the workspace's device status word:
+ * PROX_OK, PROX_ERR_TIMEOUT or PROX_ERR_BOUNDS (or PROX_ERR_CUDA if the wait failed). */
+int prox_get_status(void* ws, void* stream);
+
+/* Text for an error code (static storage). */
+const char* prox_error_string(int code);
+
+/* Test hook: the same input-selection and Stage-1 kernels as prox_build_mask, also storing
+ * the exact integer intermediates (technical summary, Stage 1 "Proxy Activation").
+ *   qx_out   [batch][d_model] int8: the activation codes (0 on rejected inputs);
+ *   sx_out   [batch][d_model/128] fp32: the activation group scales;
+ *   acc_gate, acc_up [batch][d_model/128][d_ff] int32: A[g][j] = sum over kept i in group g
+ *            of qx_i * q[j][i] (zeroed by the call, then accumulated);
+ *   salience [batch][d_ff] fp32: |SiLU(g~) * u~|.
+ * Any of the outputs may be NULL. */
+int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double input_sparsity,
+                      int8_t* qx_out, float* sx_out, int32_t* acc_gate, int32_t* acc_up,
+                      float* salience, void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook for the batch path: the ascending union of the rows of idx [batch][k]
+ * (device int32) and, per union entry, a bit mask of the tokens that selected it.
+ *   union_out [d_ff] int32, bits_out [d_ff] uint32, count_out [1] int32: device. */
+int prox_debug_union(const int32_t* idx, int batch, int k, int d_ff,
+                     int32_t* union_out, uint32_t* bits_out, int32_t* count_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook for the bounded waits: launches one block that waits on a barrier nothing ever
+ * completes, giving up after about `spin_cycles` SM clock cycles. It then records
+ * PROX_ERR_TIMEOUT in the workspace's status word and returns; no GPU fault is involved. */
+int prox_debug_wait_timeout(void* ws, size_t ws_bytes, long long spin_cycles, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PROX_H_ */
