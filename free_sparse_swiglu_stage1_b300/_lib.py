@@ -39,6 +39,7 @@ SIGNATURES = {
     "prox_sparse_ffn": (_i, [_P, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp]),
     "prox_ffn_forward": (_i, [_P, _vp, _i, _d, _d, _vp, _vp, _vp, _sz, _vp]),
     "prox_ffn_forward_host": (_i, [_P, _vp, _i, _d, _d, _vp, _vp, _sz, _vp]),
+    "prox_sparse_ffn_noalloc": (_i, [_P, _vp, _i, _vp, _i, _vp, _vp, _vp]),
     "prox_dense_ffn": (_i, [_P, _vp, _i, _vp, _vp, _sz, _vp]),
     "prox_rmsnorm": (_i, [_vp, _vp, _i, _i, _f, _vp]),
     "prox_get_status": (_i, [_vp, _vp]),

@@ -153,6 +153,30 @@ def prox_sparse_ffn(layer: PackedLayer, x: torch.Tensor, idx: torch.Tensor, ws: 
     return y
 
 
+def prox_sparse_ffn_noalloc(layer: PackedLayer, x: torch.Tensor, idx: torch.Tensor,
+                            y: torch.Tensor | None = None, stream=None,
+                            wait_status: bool = False) -> torch.Tensor:
+    """prox_sparse_ffn with the library's own fixed device scratch instead of a workspace
+    (for callers that cannot allocate one). With wait_status, waits and raises on a device
+    error."""
+    px, B = _x(layer, x)
+    if idx.dim() == 1:
+        idx = idx.view(1, -1)
+    pi = _dev(idx, torch.int32, "idx", 2)
+    if idx.shape[0] != B:
+        raise ValueError("idx must be [batch, k]")
+    if y is None:
+        y = torch.empty((B, layer.d_model), dtype=torch.float32, device=x.device)
+    py = _dev(y, torch.float32, "y")
+    st = ctypes.c_int(0)
+    _lib.check(_lib.lib().prox_sparse_ffn_noalloc(layer.ref, px, B, pi, idx.shape[1], py,
+                                                  ctypes.byref(st) if wait_status else None,
+                                                  _stream(stream, x.device)),
+               "prox_sparse_ffn_noalloc")
+    _lib.check(st.value, "prox_sparse_ffn_noalloc (device status)")
+    return y
+
+
 def prox_ffn_forward(layer: PackedLayer, x: torch.Tensor, sparsity: float, input_sparsity: float,
                      ws: Workspace, y: torch.Tensor | None = None,
                      idx_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
@@ -268,5 +292,6 @@ __all__ = [
     "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",
     "prox_k_for", "prox_pack_weights", "prox_packed_bytes", "prox_rmsnorm", "prox_sparse_ffn",
+    "prox_sparse_ffn_noalloc",
     "prox_workspace", "prox_workspace_bytes", "prox_workspace_init",
 ]

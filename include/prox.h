@@ -140,6 +140,33 @@ int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch,
                           double sparsity, double input_sparsity,
                           float* y_host, void* ws, size_t ws_bytes, void* stream);
 
+/* Bytes of the library's own device scratch used by prox_sparse_ffn_noalloc. */
+#define PROX_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* prox_sparse_ffn without a workspace, for callers that cannot allocate device memory for
+ * one: for example a serving runtime that has already reserved all device memory for its
+ * own pool, or a latency-critical loop that cannot afford the implicit synchronization of
+ * cudaMalloc. The pages have no counterpart to this call; it only changes where the
+ * scratch lives, not what is computed. Arguments and result are those of prox_sparse_ffn
+ * (same kernels, same bits).
+ *   Scratch: a fixed array of PROX_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, held
+ *   by every GPU that loads the library until the process exits. A call needs
+ *   256 + 8*d_ff + SMs * tile * d_model * 4 bytes (rounded to 256-byte pieces), where tile
+ *   is the batch's token tile (1 for one token, 2 for two, up to 4 when d_model <= 4096);
+ *   with 148 SMs that allows one token up to d_model 8192. Larger requests return
+ *   PROX_ERR_WORKSPACE before anything is launched.
+ *   Set-up: the first call on each device looks up the array's device address (with that
+ *   device current) and caches it; make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and the array keeps the last
+ *   call's contents (each call clears what must start at zero). Calls whose work overlaps
+ *   on the GPU -- on different streams, or from different threads -- race on it and must
+ *   be serialized by the caller.
+ *   status_out: if not NULL, the call waits for `stream` and stores the device status
+ *   (PROX_OK, PROX_ERR_BOUNDS, PROX_ERR_TIMEOUT) there; if NULL the call stays asynchronous.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library routine). */
+int prox_sparse_ffn_noalloc(const prox_packed* w, const float* x, int batch, const int32_t* idx,
+                            int k, float* y, int* status_out, void* stream);
+
 /* Dense SwiGLU FFN over every channel with the same kernel and weights (the baseline a
  * sparse call is compared with; technical summary, "Problem Statement"). */
 int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y,
