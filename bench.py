@@ -199,17 +199,21 @@ def profiled_traffic(kernel: str) -> tuple[float | None, str | None]:
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 
 
-def timed_graph_replays(torch, stream, graphs, barrier):
+def timed_graph_replays(torch, stream, graphs, barrier, name):
+    """Seconds for replaying `graphs` on `stream`, by CUDA events on that stream. The replays
+    sit in an NVTX range called `name`, so a profiler can be limited to them."""
     barrier()
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push(name)
     with torch.cuda.stream(stream):   # replays go to the stream the events are on
         start.record(stream)
         for g in graphs:
             g.replay()
         end.record(stream)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier()
     return start.elapsed_time(end) / 1000.0
 
@@ -329,17 +333,17 @@ def run_ours(args):
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
-    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier))
+    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier, "timed_fwd"))
     clocks = sampler.stop()
     del g_fwd
 
     K2 = min(K, 20000)
     g_s2 = graphs_for(step_s2, K2)
-    t_s2 = max_over_ranks(timed_graph_replays(torch, stream, g_s2, barrier))
+    t_s2 = max_over_ranks(timed_graph_replays(torch, stream, g_s2, barrier, "timed_stage2"))
     del g_s2
     Kd = min(K, 5000)
     g_d = graphs_for(step_dense, Kd)
-    t_dense = max_over_ranks(timed_graph_replays(torch, stream, g_d, barrier))
+    t_dense = max_over_ranks(timed_graph_replays(torch, stream, g_d, barrier, "timed_dense"))
     del g_d
 
     # end to end through the host-buffer entry point: H2D of x, the path, D2H of y, each step
