@@ -16,7 +16,13 @@ class ProxError(RuntimeError):
 
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {error_string(code)} ({code})")
+        detail = ""
+        if code == -3:   # PROX_ERR_CUDA: say which CUDA call failed and how
+            try:
+                detail = f" [{lib().prox_last_cuda_error().decode()}]"
+            except Exception:
+                pass
+        super().__init__(f"{where}: {error_string(code)} ({code}){detail}")
 
 
 class prox_packed(ctypes.Structure):
@@ -44,8 +50,10 @@ SIGNATURES = {
     "prox_rmsnorm": (_i, [_vp, _vp, _i, _i, _f, _vp]),
     "prox_get_status": (_i, [_vp, _vp]),
     "prox_error_string": (ctypes.c_char_p, [_i]),
+    "prox_last_cuda_error": (ctypes.c_char_p, []),
     "prox_debug_stage1": (_i, [_P, _vp, _i, _d, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_union": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "prox_debug_fused_forward": (_i, [_P, _vp, _d, _d, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_wait_timeout": (_i, [_vp, _sz, ctypes.c_longlong, _vp]),
 }
 

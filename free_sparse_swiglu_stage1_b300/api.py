@@ -266,6 +266,24 @@ def prox_debug_stage1(layer: PackedLayer, x: torch.Tensor, input_sparsity: float
     return out
 
 
+def prox_debug_fused_forward(layer: PackedLayer, x: torch.Tensor, sparsity: float,
+                             input_sparsity: float, ws: Workspace, stream=None):
+    """(y [1, d], selected channels [k]) of the single-token path whose Stage 2 selects its
+    channels itself; the channels come as the sure ones then the boundary winners."""
+    px, B = _x(layer, x)
+    if B != 1:
+        raise ValueError("one token")
+    k = prox_k_for(sparsity, layer.d_ff)
+    y = torch.empty((1, layer.d_model), dtype=torch.float32, device=x.device)
+    sel = torch.full((k,), -1, dtype=torch.int32, device=x.device)
+    _lib.check(_lib.lib().prox_debug_fused_forward(layer.ref, px, float(sparsity),
+                                                   float(input_sparsity), y.data_ptr(),
+                                                   sel.data_ptr(), ws.ptr, ws.nbytes,
+                                                   _stream(stream, x.device)),
+               "prox_debug_fused_forward")
+    return y, sel
+
+
 def prox_debug_union(idx: torch.Tensor, d_ff: int, ws: Workspace, stream=None):
     """(union [n] int32, bits [n] uint32-as-int32) of the rows of idx [batch, k]."""
     pi = _dev(idx, torch.int32, "idx", 2)
@@ -289,7 +307,7 @@ def prox_debug_wait_timeout(ws: Workspace, spin_cycles: int, stream=None) -> Non
 
 __all__ = [
     "GROUP", "MAX_BATCH", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
-    "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
+    "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",
     "prox_k_for", "prox_pack_weights", "prox_packed_bytes", "prox_rmsnorm", "prox_sparse_ffn",
     "prox_sparse_ffn_noalloc",

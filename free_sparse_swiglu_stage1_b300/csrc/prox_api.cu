@@ -12,7 +12,7 @@ using namespace prox;
 namespace {
 
 constexpr int kMaxDModel = 16384;
-constexpr int kMaxDff = 57344;   // the top-k block keeps one salience row in shared memory
+constexpr int kMaxDff = 53248;   // the top-k block keeps one salience row in shared memory
 
 bool shape_ok(int d, int F) {
     return d >= 128 && d <= kMaxDModel && d % 128 == 0 && F >= 32 && F <= kMaxDff && F % 32 == 0;
@@ -96,6 +96,9 @@ struct Debug {
     float* salience = nullptr;
 };
 
+// Test hook of the single-token path whose Stage 2 selects its channels itself.
+int32_t* g_fused_sel = nullptr;
+
 // The whole path over all tiles. y == nullptr stops after the mask.
 int run_path(const prox_packed* w, const float* x, int B, double sparsity, double in_sparsity,
              float* y, int32_t* idx_out, uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s,
@@ -128,7 +131,17 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
                                dbg && dbg->acc_up ? dbg->acc_up + static_cast<size_t>(t0) * G * F : nullptr,
                                sms, s));
         if (dbg) continue;
-        PROX_TRY(launch_topk(sigma + static_cast<size_t>(t0) * F, F, nb, k, idx_t, s));
+        if (g_fused_sel && y && !idx_out && nb == 1 && stage2_select_supported(d, F)) {
+            // one token, mask not wanted: Stage 2 selects its channels itself
+            PROX_TRY(launch_stage2_select(packed, L, d, F, xt, sigma + static_cast<size_t>(t0) * F,
+                                          reinterpret_cast<const int*>(ws + W.ghist), k,
+                                          y + static_cast<size_t>(t0) * d, g_fused_sel, ws, W, sms,
+                                          s));
+            continue;
+        }
+        PROX_TRY(launch_topk(sigma + static_cast<size_t>(t0) * F, F, nb, k, idx_t,
+                             reinterpret_cast<const int*>(ws + W.ghist),
+                             &reinterpret_cast<Control*>(ws + W.control)->status, s));
         if (y)
             PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, false, y + static_cast<size_t>(t0) * d,
                                      ws, W, sms, s));
@@ -158,8 +171,7 @@ int prox_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     const size_t need = ws_control_bytes((kMaxDff + 127) / 128);
     if (ws_bytes < align_up(sizeof(Control))) return PROX_ERR_WORKSPACE;
     const size_t n = ws_bytes < need ? ws_bytes : need;
-    return cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PROX_OK
-                                                                                       : PROX_ERR_CUDA;
+    return cuda_ok(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)), "clearing the workspace");
 }
 
 int prox_k_for(double sparsity, int n) {
@@ -254,10 +266,10 @@ int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch, 
     float* xd = reinterpret_cast<float*>(wsb + W.xbuf);
     float* yd = reinterpret_cast<float*>(wsb + W.ybuf);
     const size_t bytes = static_cast<size_t>(batch) * w->d_model * sizeof(float);
-    if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return PROX_ERR_CUDA;
+    PROX_TRY(cuda_ok(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s), "copying x to the device"));
     PROX_TRY(run_path(w, xd, batch, sparsity, input_sparsity, yd, nullptr, wsb, W, sms, s, nullptr));
-    if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return PROX_ERR_CUDA;
-    return cudaStreamSynchronize(s) == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    PROX_TRY(cuda_ok(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s), "copying y to the host"));
+    return cuda_ok(cudaStreamSynchronize(s), "waiting for the stream");
 }
 
 int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, void* ws,
@@ -290,13 +302,15 @@ int prox_get_status(void* ws, void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int host = 0;
     Control* ctrl = static_cast<Control*>(ws);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PROX_ERR_CUDA;
-    if (cudaMemcpyAsync(&host, &ctrl->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return PROX_ERR_CUDA;
-    if (cudaMemsetAsync(&ctrl->status, 0, sizeof(int), s) != cudaSuccess) return PROX_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return PROX_ERR_CUDA;
+    PROX_TRY(cuda_ok(cudaStreamSynchronize(s), "waiting for the stream"));
+    PROX_TRY(cuda_ok(cudaMemcpyAsync(&host, &ctrl->status, sizeof(int), cudaMemcpyDeviceToHost, s),
+                     "reading the status word"));
+    PROX_TRY(cuda_ok(cudaMemsetAsync(&ctrl->status, 0, sizeof(int), s), "clearing the status word"));
+    PROX_TRY(cuda_ok(cudaStreamSynchronize(s), "waiting for the stream"));
     return host;
 }
+
+const char* prox_last_cuda_error(void) { return last_cuda_error(); }
 
 const char* prox_error_string(int code) {
     switch (code) {
@@ -323,8 +337,8 @@ int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double in
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t acc_bytes = static_cast<size_t>(batch) * (w->d_model / 128) * w->d_ff * 4;
-    if (acc_gate && cudaMemsetAsync(acc_gate, 0, acc_bytes, s) != cudaSuccess) return PROX_ERR_CUDA;
-    if (acc_up && cudaMemsetAsync(acc_up, 0, acc_bytes, s) != cudaSuccess) return PROX_ERR_CUDA;
+    if (acc_gate) PROX_TRY(cuda_ok(cudaMemsetAsync(acc_gate, 0, acc_bytes, s), "clearing acc_gate"));
+    if (acc_up) PROX_TRY(cuda_ok(cudaMemsetAsync(acc_up, 0, acc_bytes, s), "clearing acc_up"));
     Debug dbg;
     dbg.qx = qx_out;
     dbg.sx = sx_out;
@@ -333,6 +347,28 @@ int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double in
     dbg.salience = salience;
     return run_path(w, x, batch, 0.5, input_sparsity, nullptr, nullptr, static_cast<uint8_t*>(ws), W,
                     sms, s, &dbg);
+}
+
+int prox_debug_fused_forward(const prox_packed* w, const float* x, double sparsity,
+                             double input_sparsity, float* y, int32_t* sel_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !y || !sel_out) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    if (k_rule(sparsity, w->d_ff) == w->d_ff || !stage2_select_supported(w->d_model, w->d_ff))
+        return PROX_ERR_UNSUPPORTED;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, 1, sms, W));
+    static std::mutex mu;   // the hook pointer is process-wide
+    std::lock_guard<std::mutex> lock(mu);
+    g_fused_sel = sel_out;
+    const int rc = run_path(w, x, 1, sparsity, input_sparsity, y, nullptr, static_cast<uint8_t*>(ws),
+                            W, sms, static_cast<cudaStream_t>(stream), nullptr);
+    g_fused_sel = nullptr;
+    return rc;
 }
 
 int prox_debug_union(const int32_t* idx, int batch, int k, int d_ff, int32_t* union_out,

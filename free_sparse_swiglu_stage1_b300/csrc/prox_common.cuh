@@ -94,6 +94,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) from global memory into L2 without
+// waiting; later copies of the same bytes then come from L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: wait for the previous grid's results / let the next grid
 // start its prologue. Both are no-ops when the launch carried no such dependency.
 __device__ __forceinline__ void grid_dep_wait() {
@@ -143,8 +149,12 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 // ---------------------------------------------------------------------------------------
 // Block-level helpers (all threads of the block must call them)
 // ---------------------------------------------------------------------------------------
+
+// Exclusive prefix sum over the block in thread order; `total` receives the block sum.
+// `wsum` is NT/32 ints of shared memory. Two barriers; the caller may reuse wsum only after
+// another barrier.
 template <int NT>
-__device__ __forceinline__ int block_exclusive_scan(int v, int* smem_warp, int& total) {
+__device__ __forceinline__ int block_exclusive_scan(int v, int* wsum, int& total) {
     constexpr int NW = NT / 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int x = v;
@@ -153,120 +163,175 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* smem_warp, int& 
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) smem_warp[warp] = x;
+    if (lane == 31) wsum[warp] = x;
     __syncthreads();
-    if (warp == 0) {
-        int w = lane < NW ? smem_warp[lane] : 0;
+    const int wv = lane < NW ? wsum[lane] : 0;
+    int before = lane < warp ? wv : 0;
+    int all = wv;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < NW) smem_warp[lane] = w;   // inclusive warp totals
+    for (int o = 16; o > 0; o >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+        all += __shfl_xor_sync(0xffffffffu, all, o);
     }
-    __syncthreads();
-    const int before = warp > 0 ? smem_warp[warp - 1] : 0;
-    total = smem_warp[NW - 1];
+    total = all;
     __syncthreads();
     return before + x - v;
 }
 
-// Radix select over n uint32 keys held in shared memory: finds T, the k-th largest key,
-// and how many keys equal to T belong to the top k (take_eq >= 1) when the ties among them
-// are given to the lowest indices. 1 <= k <= n. `hist` is 256 ints of shared memory,
-// `sel` 4 ints of shared memory.
+// Length of the contiguous run of keys each thread owns in the block-wide selections: a
+// power of two, at least 4 (so runs are read as 16-byte vectors).
+__host__ __device__ inline int select_run(int n, int nt) {
+    const int need = (n + nt - 1) / nt;
+    int r = 4;
+    while (r < need) r <<= 1;
+    return r;
+}
+
+// Over the bins of histogram h taken in descending order, finds the bin where the running
+// count reaches `remaining` (1 <= remaining <= total). Writes sel[0] = that bin, sel[1] = the
+// count in the bins above it, sel[2] = the count in the bin. nbins <= 2048, a multiple of NT
+// or at most NT. Two barriers; every thread calls it; sel and wsum are shared memory
+// (wsum NT/32 ints, sel 3 ints), read sel only after the call.
 template <int NT>
-__device__ void block_radix_select(const uint32_t* keys, int n, int k, int* hist, int* sel,
-                                   uint32_t& T, int& take_eq) {
-    const int tid = threadIdx.x, lane = tid & 31;
+__device__ __forceinline__ void block_find_bin(const int* h, int nbins, int remaining, int* wsum,
+                                               int* sel) {
+    constexpr int NW = NT / 32;
+    constexpr int BPT = 2048 / NT > 0 ? 2048 / NT : 1;   // bins per thread at most
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int cnt[BPT], local = 0;
+#pragma unroll
+    for (int m = 0; m < BPT; ++m) {
+        const int r = tid * BPT + m;
+        cnt[m] = r < nbins ? h[nbins - 1 - r] : 0;
+        local += cnt[m];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = (lane < warp && lane < NW) ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    const int excl = before + incl - local;
+    if (excl < remaining && excl + local >= remaining) {
+        int runc = excl;
+#pragma unroll
+        for (int m = 0; m < BPT; ++m) {
+            if (runc < remaining && runc + cnt[m] >= remaining) {
+                sel[0] = nbins - 1 - (tid * BPT + m);
+                sel[1] = runc;
+                sel[2] = cnt[m];
+            }
+            runc += cnt[m];
+        }
+    }
+    __syncthreads();
+}
+
+// Radix select over n keys (bit 31 clear, n a multiple of 4) held in shared memory, in three
+// passes of 11, 11 and 9 bits. Thread t scans the run [t*RUN, t*RUN + RUN). Finds T, the k-th
+// largest key (1 <= k <= n); take_eq, how many keys equal to T belong to the top k when ties
+// go to the lowest indices; and eq_total, how many keys equal T. `hist` is 2 * 2048 ints and
+// `wsum` NT/32 + 4 ints of shared memory. If hist0 is not null it holds the first pass's
+// 2048-bin histogram of the keys' bits 30..20 (built by whoever produced the keys), and that
+// pass only reads it.
+// If hist_ready, hist[0, 2048) already holds that first-pass histogram in shared memory.
+template <int NT, int RUN>
+__device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, int* wsum,
+                                 uint32_t& T, int& take_eq, int& eq_total,
+                                 const int* hist0 = nullptr, bool hist_ready = false) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x;
+    const int lo = tid * RUN;
+    const int nv = lo < n ? (n - lo < RUN ? n - lo : RUN) : 0;   // keys in this thread's run
+    int* sel = wsum + NW;
     uint32_t prefix = 0, pmask = 0;
     int remaining = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += NT) hist[b] = 0;
+    if (!hist_ready) {
+        for (int i = tid; i < 2048; i += NT) hist[i] = hist0 ? __ldcg(hist0 + i) : 0;
         __syncthreads();
-        for (int base = 0; base < n; base += NT) {
-            const int i = base + tid;
-            const bool act = i < n && ((keys[i] & pmask) == prefix);
-            const unsigned amask = __ballot_sync(0xffffffffu, act);
-            if (act) {
-                const int dig = (keys[i] >> shift) & 255;
-                const unsigned peers = __match_any_sync(amask, dig);
-                if (lane == __ffs(peers) - 1) atomicAdd(&hist[dig], __popc(peers));
-            }
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane L owns digits 255-8L .. 248-8L (descending); find the digit where the
-            // running count from the top reaches `remaining`
-            int cnt[8], s = 0;
+    }
+    const bool first_ready = hist_ready || hist0;
+#pragma unroll 1
+    for (int p = 0; p < 3; ++p) {
+        const int shift = p == 0 ? 20 : (p == 1 ? 9 : 0);
+        const int nbins = p == 2 ? 512 : 2048;
+        const uint32_t dmask = static_cast<uint32_t>(nbins - 1);
+        int* h = hist + (p & 1) * 2048;
+        if (p > 0 || !first_ready) {
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                cnt[m] = hist[255 - 8 * lane - m];
-                s += cnt[m];
-            }
-            int incl = s;
+            for (int i4 = 0; i4 < RUN / 4; ++i4) {
+                if (4 * i4 < nv) {
+                    const uint4 kk = *reinterpret_cast<const uint4*>(keys + lo + 4 * i4);
+                    const uint32_t k4[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const int excl = incl - s;
-            if (excl < remaining && incl >= remaining) {
-                int run = excl;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    if (run < remaining && run + cnt[m] >= remaining) {
-                        sel[0] = 255 - 8 * lane - m;
-                        sel[1] = run;
-                    }
-                    run += cnt[m];
+                    for (int m = 0; m < 4; ++m)
+                        if ((k4[m] & pmask) == prefix) atomicAdd(&h[(k4[m] >> shift) & dmask], 1);
                 }
             }
         }
+        if (p < 2) {   // clear the other buffer for the next pass
+            int* h2 = hist + ((p + 1) & 1) * 2048;
+            for (int i = tid; i < 2048; i += NT) h2[i] = 0;
+        }
         __syncthreads();
-        const int dig = sel[0];
+        block_find_bin<NT>(h, nbins, remaining, wsum, sel);
+        const uint32_t dig = static_cast<uint32_t>(sel[0]);
         remaining -= sel[1];
-        prefix |= static_cast<uint32_t>(dig) << shift;
-        pmask |= 255u << shift;
-        __syncthreads();
+        eq_total = sel[2];
+        prefix |= dig << shift;
+        pmask |= dmask << shift;
     }
     T = prefix;
     take_eq = remaining;
+    __syncthreads();   // sel and wsum are free again
 }
 
-// Writes, in ascending index order, every i with keys[i] > T plus the first take_eq
-// indices with keys[i] == T. Each thread scans a contiguous run of indices.
-// Never writes more than max_out entries. Returns the number selected (== k).
-// `scan_smem` is NT/32 ints of shared memory.
-template <int NT>
-__device__ int block_compact_topk(const uint32_t* keys, int n, uint32_t T, int take_eq,
-                                  int32_t* out, int max_out, int* scan_smem) {
-    const int tid = threadIdx.x;
-    const int per = (n + NT - 1) / NT;
-    const int lo = min(n, tid * per), hi = min(n, lo + per);
-    int eq = 0;
-    for (int i = lo; i < hi; ++i) eq += keys[i] == T;
-    int eq_total;
-    int eq_before = block_exclusive_scan<NT>(eq, scan_smem, eq_total);
+// Marks the top k given (T, take_eq, eq_total) from block_select_kth: a key is taken if it
+// is above T, or equal to T and among the first take_eq equal keys in index order. Thread t
+// owns the run [t*RUN, t*RUN + RUN) (RUN <= 64); `take` receives one bit per element of the
+// run. Returns the number taken in the run. `wsum` as for the scan.
+template <int NT, int RUN>
+__device__ __forceinline__ int block_take_topk(const uint32_t* keys, int n, uint32_t T,
+                                               int take_eq, int eq_total, int* wsum,
+                                               uint64_t& take) {
+    const int lo = static_cast<int>(threadIdx.x) * RUN;
+    const int nv = lo < n ? (n - lo < RUN ? n - lo : RUN) : 0;
+    int e = 0;
+    if (take_eq != eq_total) {   // only a partial tie needs the rank of equal keys
+        int eq = 0;
+#pragma unroll
+        for (int i = 0; i < RUN; ++i)
+            if (i < nv) eq += keys[lo + i] == T;
+        int eq_all;
+        e = block_exclusive_scan<NT>(eq, wsum, eq_all);
+    }
+    take = 0ull;
     int cnt = 0;
-    {
-        int e = eq_before;
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t kk = keys[i];
-            if (kk > T) ++cnt;
-            else if (kk == T) { cnt += e < take_eq; ++e; }
+#pragma unroll
+    for (int i4 = 0; i4 < RUN / 4; ++i4) {
+        if (4 * i4 < nv) {
+            const uint4 kk = *reinterpret_cast<const uint4*>(keys + lo + 4 * i4);
+            const uint32_t k4[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                bool t = k4[m] > T;
+                if (k4[m] == T) {
+                    t = e < take_eq;
+                    ++e;
+                }
+                if (t) {
+                    take |= 1ull << (4 * i4 + m);
+                    ++cnt;
+                }
+            }
         }
     }
-    int total;
-    int pos = block_exclusive_scan<NT>(cnt, scan_smem, total);
-    int e = eq_before;
-    for (int i = lo; i < hi; ++i) {
-        const uint32_t kk = keys[i];
-        bool take = kk > T;
-        if (kk == T) { take = e < take_eq; ++e; }
-        if (take && pos < max_out) out[pos++] = i;
-    }
-    return total;
+    return cnt;
 }
 
 }  // namespace prox

@@ -28,63 +28,80 @@ inline PackedLayout packed_layout(int d, int F) {
 // registers; wider rows leave room for fewer tokens per tile.
 inline int tile_tokens(int d) { return d <= 4096 ? 4 : (d <= 8192 ? 2 : 1); }
 
-// Stage-1 split of the kept rows (blocks of 128 channels x S row slices), bounded so the
-// partial buffer stays small: nblk * S <= 8 * SMs.
-inline int stage1_splits(int nblk, int nrows_est, int sms) {
-    int S = (4 * sms + nblk / 2) / nblk;
-    S = S < 1 ? 1 : S;
-    const int smax = (8 * sms) / nblk;
-    if (S > smax) S = smax < 1 ? 1 : smax;
-    const int by_rows = nrows_est / 64;   // keep >= 8 rows per warp
-    if (S > by_rows) S = by_rows < 1 ? 1 : by_rows;
-    return S;
+// Stage 1 work split. A warp reads one kept input row's codes for 32 * CPL channels with
+// one load of CPL bytes per lane (CPL = 16 for one token, 8 for two, 4 for four: the
+// per-token integer sums of a lane's channels stay in registers). A block of 8 warps owns
+// one tile of 32 * CPL channels and a slice of consecutive groups of 128 inputs; all blocks
+// should be resident at once (two per SM).
+struct Stage1Plan {
+    int CPL, tiles, S, gps;   // channels per lane, channel tiles, group slices, groups per slice
+};
+inline Stage1Plan stage1_plan(int d, int F, int TB, int sms) {
+    Stage1Plan pl;
+    const int G = d / 128;
+    pl.CPL = TB <= 1 ? 16 : (TB == 2 ? 8 : 4);
+    pl.tiles = (F + 32 * pl.CPL - 1) / (32 * pl.CPL);
+    int S = (2 * sms) / pl.tiles;   // tiles * S <= 2 * sms: one wave
+    S = S < 1 ? 1 : (S > G ? G : S);
+    pl.gps = (G + S - 1) / S;
+    pl.S = (G + pl.gps - 1) / pl.gps;
+    return pl;
 }
-inline int stage1_splits_max(int nblk, int sms) {
-    const int smax = (8 * sms) / nblk;
-    return smax < 1 ? 1 : smax;
+// bytes of Stage-1 partial sums any tile of up to TBmax tokens needs
+inline size_t stage1_part_bytes(int d, int F, int TBmax, int sms) {
+    size_t m = 0;
+    for (int tb = 1; tb <= TBmax; tb <<= 1) {
+        const Stage1Plan pl = stage1_plan(d, F, tb, sms);
+        const size_t b = static_cast<size_t>(pl.S) * tb * F * 16;
+        m = b > m ? b : m;
+    }
+    return m;
 }
 
-// Stage-2 pipeline: one stage = the three rows of one channel (6 d bytes).
+// Stage-2 pipeline: one stage = the three rows of one channel (6 d bytes); the number of
+// stages is a power of two so ring positions and phases are shifts and masks.
 constexpr size_t kStage2SmemBudget = 200 * 1024;
-inline int stage2_nstage(int d) {
-    int n = static_cast<int>(kStage2SmemBudget / (static_cast<size_t>(6) * d));
-    return n > 16 ? 16 : (n < 2 ? 2 : n);
+constexpr int kStage2ListMax = 1024;   // channels one block may own (indices staged in smem)
+inline int stage2_nstage_log2(int d) {
+    const size_t per = static_cast<size_t>(6) * d;
+    int lg = 1;
+    while (lg < 4 && (per << (lg + 1)) <= kStage2SmemBudget) ++lg;
+    return lg;   // 2 .. 16 stages
 }
-inline int stage2_batch(int nstage) { return nstage >= 8 ? 4 : (nstage >= 4 ? 2 : 1); }
-// 16-byte column chunks per consumer thread: blocks stay at <= 512 consumers
-inline int stage2_cpt(int d) { return d <= 2048 ? 1 : (d <= 8192 ? 2 : 4); }
-inline int stage2_consumers(int d) {
-    const int chunks = d / 8;
-    const int cpt = stage2_cpt(d);
-    int nt = (chunks / cpt + 31) / 32 * 32;
-    return nt < 32 ? 32 : nt;
+// blocks of the Stage-2 grid: one per SM, more if a block would own too many channels
+inline int stage2_blocks(int F, int sms) {
+    const int need = (F + kStage2ListMax - 1) / kStage2ListMax;
+    return sms > need ? sms : need;
 }
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, s1_cnt, xbuf, ybuf, rows, qxt, sx, gstart, s1part, sigma, idx, ulist, ubits,
-        ypart, total;
-    int TB, S_max, P, nblk;
+    size_t control, s1_cnt, xbuf, ybuf, grows, gqx, gcnt, sx, ghist, s1part, sigma, idx, ulist,
+        ubits, ypart, total;
+    int TB, P, ntile_max;
 };
 
+// Workspace of one call shape. Stage-1 inputs are kept per group of 128 inputs: grows [G][128]
+// (the group's kept inputs, ascending, padded to a multiple of 4 with copies of the last),
+// gcnt [G] (padded counts), gqx [TB][G][128] int8 codes, sx [TB][G] scales.
 inline WsLayout ws_layout(int d, int F, int B, int sms) {
     WsLayout W;
     const int G = d / 128;
     W.TB = tile_tokens(d);
-    W.nblk = (F + 127) / 128;
-    W.S_max = stage1_splits_max(W.nblk, sms);
-    W.P = sms;
+    W.ntile_max = (F + 127) / 128;
+    W.P = stage2_blocks(F, sms);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     W.control = take(sizeof(Control));
-    W.s1_cnt = take(static_cast<size_t>(W.nblk) * 4);
+    W.s1_cnt = take(static_cast<size_t>(W.ntile_max) * 4);
     W.xbuf = take(static_cast<size_t>(B) * d * 4);
     W.ybuf = take(static_cast<size_t>(B) * d * 4);
-    W.rows = take(static_cast<size_t>(d) * 4);
-    W.qxt = take(static_cast<size_t>(d) * 4);
+    W.grows = take(static_cast<size_t>(d) * 4);
+    W.gqx = take(static_cast<size_t>(W.TB) * d);
+    W.gcnt = take(static_cast<size_t>(G) * 4);
     W.sx = take(static_cast<size_t>(W.TB) * G * 4);
-    W.gstart = take(static_cast<size_t>(G + 2) * 4);
-    W.s1part = take(static_cast<size_t>(W.S_max) * W.TB * F * 16);
+    W.ghist = take(static_cast<size_t>(W.TB) * 2048 * 4);
+    W.s1part = take(stage1_part_bytes(d, F, W.TB, sms));
     W.sigma = take(static_cast<size_t>(B) * F * 4);
     W.idx = take(static_cast<size_t>(B) * F * 4);
     W.ulist = take(static_cast<size_t>(F) * 4);
@@ -95,13 +112,48 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
 }
 
 // Bytes of the control region that prox_workspace_init clears (control block + counters).
-inline size_t ws_control_bytes(int nblk) { return align_up(sizeof(Control)) + align_up(nblk * 4); }
+inline size_t ws_control_bytes(int ntile) { return align_up(sizeof(Control)) + align_up(ntile * 4); }
 
 // ------------------------------------------------------------------ launches
+// Records a failed CUDA call (the error and what was being done) for prox_last_cuda_error;
+// returns PROX_ERR_CUDA so callers can `return cuda_fail(...)`.
+int cuda_fail(cudaError_t err, const char* what);
+const char* last_cuda_error();
+inline int cuda_ok(cudaError_t err, const char* what) {
+    return err == cudaSuccess ? PROX_OK : cuda_fail(err, what);
+}
+
+// Raises `fn`'s dynamic shared-memory limit on the current device to at least `bytes`. The
+// limit is a per-function, per-device setting that the runtime checks against static plus
+// dynamic shared memory, so every launch with dynamic shared memory goes through here; the
+// largest value set so far is cached, so the runtime is called only when a launch needs more.
+int ensure_dynamic_smem(const void* fn, size_t bytes);
+
+// Launches `kernel` with programmatic dependent launch: its blocks may be scheduled while the
+// previous kernel on the stream finishes, and each kernel calls grid_dep_wait() before it
+// touches anything an earlier kernel writes.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    return err == cudaSuccess ? PROX_OK : cuda_fail(err, "kernel launch");
+}
+
 int launch_pack(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down, int d,
                 int F, const PackedLayout& L, uint8_t* base, cudaStream_t s);
 
 // Input selection + activation quantization for one tile of nb tokens (Stage 1 inputs).
+// Also clears the tile's salience histograms (ws + W.ghist) that Stage 1 fills for the top-k.
 int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, const WsLayout& W,
                        int8_t* dbg_qx, float* dbg_sx, cudaStream_t s);
 
@@ -110,9 +162,10 @@ int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, in
                   uint8_t* ws, const WsLayout& W, float* sigma_tile, int32_t* dbg_gate,
                   int32_t* dbg_up, int sms, cudaStream_t s);
 
-// Per-token top-k of the salience -> ascending channel indices (row stride k).
+// Per-token top-k of the salience -> ascending channel indices (row stride k). ghist, if not
+// null, holds per token the 2048-bin histogram of the salience bits 30..20 (Stage 1 builds it).
 int launch_topk(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
-                cudaStream_t s);
+                const int* ghist, int* status, cudaStream_t s);
 
 // Union of nb index rows (row stride k) -> ascending list + per-entry token bits + count.
 int launch_union(const int32_t* idx_tile, int nb, int k, int F, int32_t* ulist, uint32_t* ubits,
@@ -123,6 +176,15 @@ int launch_stage2(const uint8_t* packed, const PackedLayout& L, int d, int F, co
                   int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
                   int count_host, float* y_tile, uint8_t* ws, const WsLayout& W, int sms,
                   cudaStream_t s);
+
+// Single-token Stage 2 that selects its channels itself from the salience and Stage 1's
+// histogram (the top-k is folded into the Stage-2 kernel's front end).
+bool stage2_select_supported(int d, int F);
+// dbg_sel (nullable): every selected channel, the sure ones then the boundary winners.
+int launch_stage2_select(const uint8_t* packed, const PackedLayout& L, int d, int F,
+                         const float* x, const float* sigma, const int* ghist, int k, float* y,
+                         int32_t* dbg_sel, uint8_t* ws, const WsLayout& W, int sms,
+                         cudaStream_t s);
 
 int launch_rmsnorm(const float* y, float* x_out, int batch, int d, float eps, cudaStream_t s);
 

@@ -1,8 +1,40 @@
 // Small kernels around the path: the unit-gain RMSNorm between stacked layers, an index
 // fill for the all-channels mask, and the bounded-wait probe used to test timeouts.
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "prox_kernels.cuh"
 
 namespace prox {
+
+namespace {
+thread_local char g_last_cuda_error[256] = "none";
+}
+
+int cuda_fail(cudaError_t err, const char* what) {
+    snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", what,
+             cudaGetErrorName(err), cudaGetErrorString(err));
+    return PROX_ERR_CUDA;
+}
+
+const char* last_cuda_error() { return g_last_cuda_error; }
+
+int ensure_dynamic_smem(const void* fn, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> done;
+    int dev = 0;
+    if (cuda_ok(cudaGetDevice(&dev), "cudaGetDevice") != PROX_OK) return PROX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = done[std::make_pair(fn, dev)];
+    if (bytes <= have && have != 0) return PROX_OK;
+    const cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(bytes));
+    if (err != cudaSuccess) return cuda_fail(err, "raising a kernel's shared-memory limit");
+    have = bytes;
+    return PROX_OK;
+}
 
 // x_out[b][:] = y[b][:] / sqrt(mean(y[b]^2) + eps); one block per row, fixed-order sum.
 __global__ void __launch_bounds__(256)
@@ -48,18 +80,18 @@ __global__ void wait_probe_kernel(int* __restrict__ status, long long spin_cycle
 
 int launch_rmsnorm(const float* y, float* x_out, int batch, int d, float eps, cudaStream_t s) {
     rmsnorm_kernel<<<batch, 256, 0, s>>>(y, x_out, d, eps);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "rmsnorm launch");
 }
 
 int launch_iota(int32_t* out, int n, int rows, cudaStream_t s) {
     const int total = n * rows;
     iota_kernel<<<(total + 255) / 256, 256, 0, s>>>(out, n, rows);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "index fill launch");
 }
 
 int launch_wait_probe(int* status, long long spin_cycles, cudaStream_t s) {
     wait_probe_kernel<<<1, 32, 0, s>>>(status, spin_cycles);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "wait probe launch");
 }
 
 }  // namespace prox

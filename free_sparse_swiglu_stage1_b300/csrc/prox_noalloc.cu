@@ -65,8 +65,7 @@ extern "C" int prox_sparse_ffn_noalloc(const prox_packed* w, const float* x, int
     W.TB = tile_tokens(d);
     const int TB = batch < W.TB ? (batch <= 1 ? 1 : (batch <= 2 ? 2 : 4)) : W.TB;
     W.TB = TB;
-    W.P = sms;
-    W.nblk = (F + 127) / 128;
+    W.P = stage2_blocks(F, sms);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     W.control = take(sizeof(Control));

@@ -3,10 +3,12 @@
 // ranking of the entries, not their values).
 //
 // topk_kernel   one block per token. The salience values are non-negative fp32, so their
-//               bit patterns order like the values and a 4-pass 8-bit radix select finds
-//               the k-th largest key T and how many keys equal to T belong to the top k.
-//               One scan in index order then emits the mask as ascending channel indices,
-//               giving equal values to the lower index.
+//               bit patterns order like the values and a three-pass radix select (11, 11
+//               and 9 bits) finds the k-th largest key T and how many keys equal to T belong
+//               to the top k; the first pass's histogram comes ready from Stage 1, so only
+//               the candidates of one bin are scanned again. One scan in index order then
+//               emits the mask as ascending channel indices, giving equal values to the
+//               lower index.
 // union_kernel  batch path: the tile's per-token masks are merged into one ascending list
 //               of channels and a bit mask per entry telling which tokens selected it, so
 //               Stage 2 reads each selected row once for the whole tile.
@@ -16,20 +18,45 @@ namespace prox {
 
 constexpr int kTopkThreads = 1024;
 
-__global__ void __launch_bounds__(kTopkThreads)
-topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__ idx) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    __shared__ int hist[256], sel[4], scan[32];
-    const int b = blockIdx.x;
-    grid_dep_wait();
-    const float* sg = sigma + static_cast<size_t>(b) * F;
-    for (int i = threadIdx.x; i < F; i += kTopkThreads) keys[i] = __float_as_uint(sg[i]);
+template <int NT, int RUN>
+__global__ void __launch_bounds__(NT)
+topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__ idx,
+            const int* __restrict__ ghist, long long spin, int* __restrict__ status) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);   // [F] salience bits (all >= 0)
+    __shared__ __align__(128) int hist[2 * 2048];
+    __shared__ int wsum[NT / 32 + 4];
+    __shared__ __align__(8) uint64_t bar;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
     __syncthreads();
+    grid_dep_wait();
+    // the token's salience row and its first-pass histogram, each one bulk copy
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(F) * 4 + 2048 * 4);
+        bulk_g2s(keys, sigma + static_cast<size_t>(b) * F, static_cast<uint32_t>(F) * 4, &bar);
+        bulk_g2s(hist, ghist + static_cast<size_t>(b) * 2048, 2048 * 4, &bar);
+    }
+    if (!mbar_wait(&bar, 0u, spin, status)) {
+        // nothing usable arrived: leave the mask unwritten; the status word says why
+        // (every thread waits on the same barrier, so all of them leave here together)
+        return;
+    }
     uint32_t T;
-    int take;
-    block_radix_select<kTopkThreads>(keys, F, k, hist, sel, T, take);
-    block_compact_topk<kTopkThreads>(keys, F, T, take, idx + static_cast<size_t>(b) * k, k, scan);
+    int take, eq_total;
+    block_select_kth<NT, RUN>(keys, F, k, hist, wsum, T, take, eq_total, nullptr, true);
+    uint64_t mine;
+    const int cnt = block_take_topk<NT, RUN>(keys, F, T, take, eq_total, wsum, mine);
+    int total;
+    int pos = block_exclusive_scan<NT>(cnt, wsum, total);
+    int32_t* out = idx + static_cast<size_t>(b) * k;
+    const int lo = tid * RUN;
+#pragma unroll
+    for (int i = 0; i < RUN; ++i)
+        if (((mine >> i) & 1ull) && pos < k) out[pos++] = lo + i;
     grid_dep_launch();
 }
 
@@ -38,7 +65,7 @@ union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __r
              uint32_t* __restrict__ ubits, int* __restrict__ count, int* __restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* bits = reinterpret_cast<uint32_t*>(smem);
-    __shared__ int scan[32];
+    __shared__ int wsum[kTopkThreads / 32 + 4];
     const int tid = threadIdx.x;
     grid_dep_wait();
     for (int i = tid; i < F; i += kTopkThreads) bits[i] = 0u;
@@ -57,7 +84,7 @@ union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __r
     int cnt = 0;
     for (int i = lo; i < hi; ++i) cnt += bits[i] != 0u;
     int total;
-    int pos = block_exclusive_scan<kTopkThreads>(cnt, scan, total);
+    int pos = block_exclusive_scan<kTopkThreads>(cnt, wsum, total);
     for (int i = lo; i < hi; ++i) {
         if (bits[i]) {
             ulist[pos] = i;
@@ -69,27 +96,34 @@ union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __r
     grid_dep_launch();
 }
 
-int launch_topk(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile, cudaStream_t s) {
+template <int NT, int RUN>
+static int launch_topk_t(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
+                         const int* ghist, int* status, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(F) * 4;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(reinterpret_cast<const void*>(topk_kernel),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return PROX_ERR_CUDA;
-    topk_kernel<<<nb, kTopkThreads, smem, s>>>(sigma_tile, F, k, idx_tile);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    auto fn = topk_kernel<NT, RUN>;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
+    return launch_pdl(fn, dim3(nb), dim3(NT), smem, s, sigma_tile, F, k, idx_tile, ghist,
+                      kDefaultSpinCycles, status);
+}
+
+int launch_topk(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
+                const int* ghist, int* status, cudaStream_t s) {
+    switch (select_run(F, 1024)) {
+        case 4: return launch_topk_t<1024, 4>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        case 8: return launch_topk_t<1024, 8>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        case 16: return launch_topk_t<1024, 16>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        case 32: return launch_topk_t<1024, 32>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        case 64: return launch_topk_t<1024, 64>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        default: return PROX_ERR_UNSUPPORTED;
+    }
 }
 
 int launch_union(const int32_t* idx_tile, int nb, int k, int F, int32_t* ulist, uint32_t* ubits,
                  int* count, int* status, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(F) * 4;
-    if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(reinterpret_cast<const void*>(union_kernel),
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return PROX_ERR_CUDA;
-    union_kernel<<<1, kTopkThreads, smem, s>>>(idx_tile, nb, k, F, ulist, ubits, count, status);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(union_kernel), smem) != PROX_OK) return PROX_ERR_CUDA;
+    return launch_pdl(union_kernel, dim3(1), dim3(kTopkThreads), smem, s, idx_tile, nb, k, F, ulist,
+                      ubits, count, status);
 }
 
 }  // namespace prox

@@ -2,29 +2,30 @@
 // INT4 proxy projections of W_gate and W_up over the kept inputs only, and the salience
 // |SiLU(g~) * u~| of every intermediate channel.
 //
-// input_quant_kernel (one block per tile of tokens)
-//   For each token: radix-select the k_in largest |x_i| (ties to the lower index), then per
-//   group of 128 inputs sx = max|x_hat| / 127 and qx = clamp(rint(x_hat / sx), -127, 127)
-//   in binary32. The union of the tile's kept inputs becomes an ascending row list; each
-//   row carries its tokens' int8 codes packed in one 32-bit word, and gstart[g] marks where
-//   group g starts in the list.
+// input_quant_kernel (one block of 1024 threads per tile of tokens)
+//   For each token: a three-pass radix select finds the k_in-th largest |x_i| (ties to the
+//   lower index); then per group of 128 inputs sx = max|x_hat| / 127 and
+//   qx = clamp(rint(x_hat / sx), -127, 127) in binary32. Per group, the inputs any token of
+//   the tile kept are listed in ascending order (padded to a multiple of 4 with copies of the
+//   last one, whose codes are 0) with every token's int8 codes; no global compaction is
+//   needed, since each group's list has a fixed place.
 //
-// stage1_kernel (grid: 128-channel blocks x S slices of the row list, 8 warps per block)
-//   The "fused split-N" design: a block owns 128 channels and a slice of the kept rows;
-//   a kept input is one contiguous 128-byte run of codes (gate | up nibbles of 128
-//   channels), read by one warp with one 32-bit load per lane, so rejected inputs cost
-//   no bytes. Lane l owns channels 4l..4l+3 of both projections.
-//   The int4 x int8 products are accumulated exactly in two 16-bit lanes of a 32-bit
-//   register: the nibble pairs (0,4), (1,5), (2,6), (3,7) of a code word are isolated with
-//   one mask each and multiplied by the activation code in a single integer multiply-add.
-//   With codes in [0, 15] and |qx| <= 127, sixteen rows fit in a signed 16-bit lane
-//   (16 * 15 * 127 = 30480 < 32768); every 16 rows the lanes are moved into int32
-//   accumulators. Codes are stored as q + 8, so the group result is corrected by
-//   -8 * sum(qx) over the same rows, which keeps every integer exact.
+// stage1_kernel (grid: channel tiles x slices of consecutive groups, 8 warps per block)
+//   The "fused split-N" design: a block owns a tile of 32 * CPL channels and the kept rows
+//   of a few groups; a kept input is one contiguous run of CPL bytes per lane (gate | up
+//   nibbles of CPL channels), so rejected inputs cost no bytes and a warp reads a row with
+//   one wide load per lane. The rows are taken four at a time (a quad never crosses a
+//   group): the four loaded words of each 4-channel column are transposed with byte
+//   permutes, so each channel's codes of the four rows sit in one word, and one dp4a per
+//   channel and projection multiplies them by the four rows' int8 codes. Gate codes enter as
+//   bytes q + 8 in [1, 15], up codes as 16 * (q + 8), and one more dp4a accumulates 8 * sum(qx)
+//   of the rows, so A = sum(q * qx) is recovered exactly per group in int32.
 //   At each group end the exact integer A is scaled by sx * sw and added to a double-float
-//   (hi, lo) sum, so g~ and u~ carry about 44 significant bits before the final fp32
-//   rounding. Warps, then row slices, are combined in a fixed order (the last block to
-//   finish a channel block does the final sum), so the result is deterministic.
+//   (hi, lo) sum in shared memory, so g~ and u~ carry about 44 significant bits before the
+//   final fp32 rounding. Warps, then group slices, are combined in a fixed order (the last
+//   block to finish a channel tile does the final sum and the salience), so the result is
+//   deterministic. That block also counts the salience's top 11 bits into a histogram the
+//   top-k starts from.
 #include "prox_kernels.cuh"
 
 namespace prox {
@@ -32,334 +33,414 @@ namespace prox {
 constexpr int kSelThreads = 1024;
 constexpr int kS1Threads = 256;
 constexpr int kS1Warps = kS1Threads / 32;
-constexpr int kRowsPerFlush = 16;
 
+// Input selection and activation codes for one tile of nb tokens (see the file comment).
+// Thread t owns the run of inputs [t*RUN, t*RUN + RUN), RUN a power of two in [4, 16], so a
+// run lies inside one group of 128 and a group's runs are 128/RUN aligned lanes of one warp.
+// Outputs: grows [G][128], gcnt [G], gqx [TB][G][128], sx [TB][G]; clears ghist [TB][2048].
+template <int RUN>
 __global__ void __launch_bounds__(kSelThreads)
 input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
-                   int* __restrict__ rows, uint32_t* __restrict__ qxt, float* __restrict__ sx_ws,
-                   int* __restrict__ gstart, int8_t* __restrict__ dbg_qx,
-                   float* __restrict__ dbg_sx) {
+                   int* __restrict__ grows, int* __restrict__ gcnt, int8_t* __restrict__ gqx,
+                   float* __restrict__ sx_ws, int* __restrict__ ghist,
+                   int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx) {
     extern __shared__ __align__(16) unsigned char smem[];
-    float* xs = reinterpret_cast<float*>(smem);
-    uint32_t* keys = reinterpret_cast<uint32_t*>(xs + d);
-    int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);
-    uint8_t* kflag = reinterpret_cast<uint8_t*>(qx8 + TB * d);
-    __shared__ int hist[256], sel[4], scan[32];
-    constexpr int NT = kSelThreads, NW = NT / 32;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                 // [d]
+    int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);                   // [TB][d]
+    __shared__ int hist[2 * 2048];
+    __shared__ int wsum[kSelThreads / 32 + 4];
+    constexpr int NT = kSelThreads;
+    constexpr int tpg = 128 / RUN;                 // threads per group (8 .. 32)
+    const int tid = threadIdx.x;
     const int G = d >> 7;
-    const int per = (d + NT - 1) / NT;
-    const int lo = min(d, tid * per), hi = min(d, lo + per);
+    const int lo = min(d, tid * RUN), hi = min(d, lo + RUN);
+    const int g_mine = lo >> 7;
+    const bool active = lo < hi;
+    const int gl = tid & (tpg - 1);                // this thread's place among its group's
 
     grid_dep_wait();
-    for (int i = tid; i < d; i += NT) kflag[i] = 0;
-    for (int i = tid; i < TB * d; i += NT) qx8[i] = 0;
-    __syncthreads();
-
+    for (int i = tid; i < TB * 512; i += NT)   // filled by Stage 1 for the top-k
+        reinterpret_cast<int4*>(ghist)[i] = make_int4(0, 0, 0, 0);
+    uint64_t any = 0ull;
     for (int b = 0; b < nb; ++b) {
-        for (int i = tid; i < d; i += NT) {
-            const float v = x[static_cast<size_t>(b) * d + i];
-            xs[i] = v;
-            keys[i] = __float_as_uint(v) & 0x7fffffffu;
+        float xv[RUN];
+#pragma unroll
+        for (int e4 = 0; e4 < RUN / 4; ++e4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (active) v = *reinterpret_cast<const float4*>(x + static_cast<size_t>(b) * d + lo + e4 * 4);
+            xv[e4 * 4] = v.x; xv[e4 * 4 + 1] = v.y; xv[e4 * 4 + 2] = v.z; xv[e4 * 4 + 3] = v.w;
+            if (active) {
+                uint4 kk;
+                kk.x = __float_as_uint(v.x) & 0x7fffffffu;
+                kk.y = __float_as_uint(v.y) & 0x7fffffffu;
+                kk.z = __float_as_uint(v.z) & 0x7fffffffu;
+                kk.w = __float_as_uint(v.w) & 0x7fffffffu;
+                *reinterpret_cast<uint4*>(keys + lo + e4 * 4) = kk;
+            }
         }
         __syncthreads();
         uint32_t T;
-        int take;
-        block_radix_select<NT>(keys, d, k_in, hist, sel, T, take);
-        // mark the kept inputs, walking contiguous runs so equal keys go to lower indices
-        int eq = 0;
-        for (int i = lo; i < hi; ++i) eq += keys[i] == T;
-        int eq_total;
-        int e = block_exclusive_scan<NT>(eq, scan, eq_total);
-        for (int i = lo; i < hi; ++i) {
-            const uint32_t kk = keys[i];
-            bool keep = kk > T;
-            if (kk == T) { keep = e < take; ++e; }
-            if (keep) kflag[i] |= static_cast<uint8_t>(1u << b);
+        int take, eq_total;
+        block_select_kth<NT, RUN>(keys, d, k_in, hist, wsum, T, take, eq_total);
+        uint64_t mine;
+        block_take_topk<NT, RUN>(keys, d, T, take, eq_total, wsum, mine);
+        any |= mine;
+        // per-group scale over the group's aligned lanes
+        float m = 0.f;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e)
+            if ((mine >> e) & 1ull) m = fmaxf(m, fabsf(xv[e]));
+        for (int o = tpg >> 1; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float sxg = __fdiv_rn(m, 127.0f);
+        uint32_t qw[RUN / 4];
+#pragma unroll
+        for (int e4 = 0; e4 < RUN / 4; ++e4) qw[e4] = 0u;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e) {
+            float q = 0.f;
+            if (((mine >> e) & 1ull) && sxg != 0.f)
+                q = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(xv[e], sxg))));
+            const uint32_t qb = static_cast<uint32_t>(static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q))));
+            qw[e >> 2] |= qb << (8 * (e & 3));
         }
-        __syncthreads();
-        // per-group scale and int8 codes of the kept inputs
-        for (int g = warp; g < G; g += NW) {
-            float xv[4];
-            bool kp[4];
-            float m = 0.f;
+        if (active) {
 #pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const int i = g * 128 + lane * 4 + mm;
-                xv[mm] = xs[i];
-                kp[mm] = (kflag[i] >> b) & 1;
-                if (kp[mm]) m = fmaxf(m, fabsf(xv[mm]));
+            for (int e4 = 0; e4 < RUN / 4; ++e4) {
+                *reinterpret_cast<uint32_t*>(qx8 + b * d + lo + e4 * 4) = qw[e4];
+                if (dbg_qx)
+                    *reinterpret_cast<uint32_t*>(dbg_qx + static_cast<size_t>(b) * d + lo + e4 * 4) = qw[e4];
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            const float sxg = __fdiv_rn(m, 127.0f);
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const int i = g * 128 + lane * 4 + mm;
-                float q = 0.f;
-                if (kp[mm] && sxg != 0.f)
-                    q = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(xv[mm], sxg))));
-                const int8_t qi = static_cast<int8_t>(static_cast<int>(q));
-                qx8[b * d + i] = qi;
-                if (dbg_qx) dbg_qx[static_cast<size_t>(b) * d + i] = qi;
-            }
-            if (lane == 0) {
-                sx_ws[b * G + g] = sxg;
-                if (dbg_sx) dbg_sx[b * G + g] = sxg;
+            if (gl == 0) {
+                sx_ws[b * G + g_mine] = sxg;
+                if (dbg_sx) dbg_sx[b * G + g_mine] = sxg;
             }
         }
-        __syncthreads();
+        __syncthreads();   // keys are rewritten for the next token
     }
     for (int i = tid; i < (TB - nb) * G; i += NT) sx_ws[nb * G + i] = 0.f;
 
-    // ascending union of the kept inputs, with the tile's codes packed per row
-    int cnt = 0;
-    for (int i = lo; i < hi; ++i) cnt += kflag[i] != 0;
-    int total;
-    int pos = block_exclusive_scan<NT>(cnt, scan, total);
-    for (int i = lo; i < hi; ++i) {
-        if ((i & 127) == 0) gstart[i >> 7] = pos;
-        if (kflag[i]) {
-            uint32_t w = 0;
-            for (int b = 0; b < TB; ++b)
-                w |= static_cast<uint32_t>(static_cast<uint8_t>(qx8[b * d + i])) << (8 * b);
-            rows[pos] = i;
-            qxt[pos] = w;
-            ++pos;
-        }
+    // per group: the inputs any token kept, ascending, then padding to a multiple of 4
+    const int cnt = __popcll(any);
+    int incl = cnt;
+    for (int o = 1; o < tpg; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o, tpg);
+        if (gl >= o) incl += y;
     }
-    if (tid == 0) {
-        gstart[G] = total;
-        gstart[G + 1] = total;
+    const int n_g = __shfl_sync(0xffffffffu, incl, tpg - 1, tpg);
+    int last = -1;
+#pragma unroll
+    for (int e = 0; e < RUN; ++e)
+        if ((any >> e) & 1ull) last = lo + e;
+    for (int o = tpg >> 1; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    if (active) {
+        int* rows_g = grows + g_mine * 128;
+        int p = incl - cnt;
+#pragma unroll
+        for (int e = 0; e < RUN; ++e) {
+            if ((any >> e) & 1ull) {
+                const int i = lo + e;
+                rows_g[p] = i;
+                for (int b = 0; b < TB; ++b)
+                    gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + p] = b < nb ? qx8[b * d + i] : 0;
+                ++p;
+            }
+        }
+        if (gl == tpg - 1) {
+            const int padded = (n_g + 3) & ~3;
+            for (int q = n_g; q < padded; ++q) {
+                rows_g[q] = last;
+                for (int b = 0; b < TB; ++b) gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + q] = 0;
+            }
+            gcnt[g_mine] = padded;
+        }
     }
     grid_dep_launch();
 }
 
-// Moves the two signed 16-bit lanes of a packed accumulator into int32 sums.
-__device__ __forceinline__ void unpack_lanes(uint32_t p, int& lo_acc, int& hi_acc) {
-    const int lo = static_cast<int>(static_cast<int16_t>(p & 0xFFFFu));
-    const int hi = static_cast<int>(p - static_cast<uint32_t>(lo)) >> 16;
-    lo_acc += lo;
-    hi_acc += hi;
+// dp4a with unsigned bytes in a and signed bytes in b
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int r;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
 }
 
-template <int TB>
-__global__ void __launch_bounds__(kS1Threads)
+// CPL bytes of codes (CPL/4 words) of one row for one lane
+template <int CPL>
+__device__ __forceinline__ void load_codes(uint32_t (&w)[CPL / 4], const uint8_t* p, bool ok) {
+    if constexpr (CPL == 16) {
+        const uint4 v = ok ? __ldg(reinterpret_cast<const uint4*>(p)) : make_uint4(0u, 0u, 0u, 0u);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (CPL == 8) {
+        const uint2 v = ok ? __ldg(reinterpret_cast<const uint2*>(p)) : make_uint2(0u, 0u);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        w[0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(p)) : 0u;
+    }
+}
+
+template <int TB, int CPL>
+__global__ void __launch_bounds__(kS1Threads, 2)
 stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ scales, int d, int F,
-              const int* __restrict__ rows, const uint32_t* __restrict__ qxt,
-              const float* __restrict__ sx, const int* __restrict__ gstart, int S, int nb,
-              float2* __restrict__ part, int* __restrict__ cnt, float* __restrict__ sigma,
-              int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up, int* __restrict__ status) {
+              const int* __restrict__ grows, const int* __restrict__ gcnt,
+              const int8_t* __restrict__ gqx, const float* __restrict__ sx, int gps, int S,
+              int nb, float2* __restrict__ part, int* __restrict__ cnt, float* __restrict__ sigma,
+              int* __restrict__ ghist, int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up,
+              int* __restrict__ status) {
+    constexpr int NV = 2 * CPL * TB;       // values per lane: (token, channel, projection)
+    constexpr int NWC = CPL / 4;           // code words per lane and row
+    constexpr int TILE = 32 * CPL;         // channels per block
     extern __shared__ __align__(16) unsigned char smem[];
-    DF* red = reinterpret_cast<DF*>(smem);                        // [warps][TB][8][32]
-    float* gu = reinterpret_cast<float*>(smem);                   // [TB][8][32] (reused)
+    int* s_A = reinterpret_cast<int*>(smem);                               // [gps][NV][32]
+    uint32_t* s_sc = reinterpret_cast<uint32_t*>(s_A + gps * NV * 32);     // [gps][TILE]
+    int* s_rows = reinterpret_cast<int*>(s_sc + gps * TILE);               // [gps][128]
+    uint32_t* s_qx = reinterpret_cast<uint32_t*>(s_rows + gps * 128);      // [TB][gps][32]
+    float* s_sx = reinterpret_cast<float*>(s_qx + TB * gps * 32);          // [TB][gps]
+    int* s_qs = reinterpret_cast<int*>(s_sx + TB * gps);                   // [gps + 1] quad starts
     __shared__ int last_flag;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tile = blockIdx.x, s = blockIdx.y;
     const int G = d >> 7;
-    const int blk = blockIdx.x, s = blockIdx.y;
-    const int j0 = blk * 128 + lane * 4;
-    const bool valid = j0 < F;
+    const int g0 = s * gps, ng = min(gps, G - g0);
+    const int c0 = tile * TILE + lane * CPL;          // this lane's first channel
+    const bool valid = c0 < F;                        // F % 16 == 0: all CPL channels or none
+    const uint8_t* cbase = codes + (valid ? c0 : 0);
 
-    grid_dep_wait();
-    const int nrows = gstart[G];
-    const int ra = static_cast<int>(static_cast<long long>(nrows) * s / S);
-    const int rb = static_cast<int>(static_cast<long long>(nrows) * (s + 1) / S);
-    const int m = rb - ra;
-    const int wa = ra + static_cast<int>(static_cast<long long>(m) * warp / kS1Warps);
-    const int wb = ra + static_cast<int>(static_cast<long long>(m) * (warp + 1) / kS1Warps);
-    const uint8_t* cbase = codes + (valid ? j0 : 0);
-
-    DF acc[TB][8];
-#pragma unroll
-    for (int b = 0; b < TB; ++b)
-#pragma unroll
-        for (int v = 0; v < 8; ++v) acc[b][v] = DF{0.f, 0.f};
-
-    int r = wa;
-    while (r < wb) {
-        const int g = rows[r] >> 7;
-        const int gend = min(wb, gstart[g + 1]);
-        if (g >= G || gend <= r) {   // inconsistent row list: record it, never spin
-            if (lane == 0) set_status(status, PROX_ERR_BOUNDS);
-            break;
-        }
-        int A[TB][8];
-        int qs[TB];
-#pragma unroll
-        for (int b = 0; b < TB; ++b) {
-            qs[b] = 0;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) A[b][v] = 0;
-        }
-        for (int c = r; c < gend; c += kRowsPerFlush) {
-            const int n = min(kRowsPerFlush, gend - c);
-            int myrow = 0;
-            uint32_t myq = 0;
-            if (lane < n) {
-                myrow = rows[c + lane];
-                myq = qxt[c + lane];
-            }
-            uint32_t w[kRowsPerFlush];
-#pragma unroll
-            for (int u = 0; u < kRowsPerFlush; ++u) {
-                const int ri = __shfl_sync(0xffffffffu, myrow, u);
-                w[u] = (u < n && valid)
-                           ? __ldg(reinterpret_cast<const uint32_t*>(cbase + static_cast<size_t>(ri) * F))
-                           : 0u;
-            }
-            uint32_t P[TB][4];
-#pragma unroll
-            for (int b = 0; b < TB; ++b)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) P[b][k] = 0u;
-#pragma unroll
-            for (int u = 0; u < kRowsPerFlush; ++u) {
-                const uint32_t qq = __shfl_sync(0xffffffffu, myq, u);
-                const uint32_t e0 = w[u] & 0x000F000Fu;          // gate c0 | gate c2
-                const uint32_t e1 = (w[u] >> 4) & 0x000F000Fu;   // up   c0 | up   c2
-                const uint32_t e2 = (w[u] >> 8) & 0x000F000Fu;   // gate c1 | gate c3
-                const uint32_t e3 = (w[u] >> 12) & 0x000F000Fu;  // up   c1 | up   c3
-#pragma unroll
-                for (int b = 0; b < TB; ++b) {
-                    const int q = static_cast<int>(static_cast<int8_t>(qq >> (8 * b)));
-                    const uint32_t uq = static_cast<uint32_t>(q);
-                    P[b][0] += e0 * uq;
-                    P[b][1] += e1 * uq;
-                    P[b][2] += e2 * uq;
-                    P[b][3] += e3 * uq;
-                    qs[b] += q;
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < TB; ++b) {
-                unpack_lanes(P[b][0], A[b][0], A[b][2]);
-                unpack_lanes(P[b][1], A[b][4], A[b][6]);
-                unpack_lanes(P[b][2], A[b][1], A[b][3]);
-                unpack_lanes(P[b][3], A[b][5], A[b][7]);
-            }
-        }
-        // group end: A - 8*sum(qx) is the exact integer proxy product over these rows
-        if (valid) {
-            const uint4 sw4 = __ldg(reinterpret_cast<const uint4*>(scales + static_cast<size_t>(g) * F + j0));
-            const uint32_t swv[4] = {sw4.x, sw4.y, sw4.z, sw4.w};
-#pragma unroll
-            for (int b = 0; b < TB; ++b) {
-                const float sxb = sx[b * G + g];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int ag = A[b][c4] - 8 * qs[b];
-                    const int au = A[b][4 + c4] - 8 * qs[b];
-                    const float swg = __half2float(__ushort_as_half(static_cast<unsigned short>(swv[c4] & 0xFFFFu)));
-                    const float swu = __half2float(__ushort_as_half(static_cast<unsigned short>(swv[c4] >> 16)));
-                    acc[b][c4] = df_add(acc[b][c4], df_scaled_int(sxb, swg, ag));
-                    acc[b][4 + c4] = df_add(acc[b][4 + c4], df_scaled_int(sxb, swu, au));
-                    if (dbg_gate && b < nb) atomicAdd(&dbg_gate[(static_cast<size_t>(b) * G + g) * F + j0 + c4], ag);
-                    if (dbg_up && b < nb) atomicAdd(&dbg_up[(static_cast<size_t>(b) * G + g) * F + j0 + c4], au);
-                }
-            }
-        }
-        r = gend;
+    // the packed weights do not depend on earlier kernels: stage this tile's scales first
+    for (int i = tid; i < ng * (TILE / 4); i += kS1Threads) {
+        const int gl = i / (TILE / 4), c4 = i - gl * (TILE / 4);
+        const int ch = tile * TILE + 4 * c4;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ch < F) v = __ldg(reinterpret_cast<const uint4*>(scales + static_cast<size_t>(g0 + gl) * F + ch));
+        reinterpret_cast<uint4*>(s_sc)[gl * (TILE / 4) + c4] = v;
     }
-
-    // combine the 8 warps in a fixed order
+    for (int i = tid; i < ng * NV * 32 / 4; i += kS1Threads)
+        reinterpret_cast<int4*>(s_A)[i] = make_int4(0, 0, 0, 0);
+    grid_dep_wait();
+    for (int i = tid; i < ng * 32; i += kS1Threads)
+        reinterpret_cast<int4*>(s_rows)[i] = __ldcg(reinterpret_cast<const int4*>(grows + g0 * 128) + i);
+    for (int i = tid; i < TB * ng * 32; i += kS1Threads) {
+        const int b = i / (ng * 32), r = i - b * (ng * 32);
+        s_qx[b * gps * 32 + r] = __ldcg(reinterpret_cast<const uint32_t*>(gqx + (static_cast<size_t>(b) * G + g0) * 128) + r);
+    }
+    for (int i = tid; i < TB * ng; i += kS1Threads) {
+        const int b = i / ng, gl = i - b * ng;
+        s_sx[b * gps + gl] = __ldcg(sx + b * G + g0 + gl);
+    }
+    if (tid < 32) {
+        // quad starts of the slice's groups: exclusive scan of gcnt / 4, 4 groups per lane
+        int c4v[4], loc = 0;
 #pragma unroll
-    for (int b = 0; b < TB; ++b)
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int gl = lane * 4 + m4;
+            int c = gl < ng ? __ldcg(gcnt + g0 + gl) : 0;
+            if (c < 0 || c > 128 || (c & 3)) {
+                set_status(status, PROX_ERR_BOUNDS);
+                c = 0;
+            }
+            c4v[m4] = c >> 2;
+            loc += c4v[m4];
+        }
+        int incl = loc;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) red[((warp * TB + b) * 8 + v) * 32 + lane] = acc[b][v];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - loc;
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int gl = lane * 4 + m4;
+            if (gl < ng) s_qs[gl] = run;
+            run += c4v[m4];
+        }
+        if (lane == 31) s_qs[ng] = incl;
+    }
     __syncthreads();
-    {
-        const int v = warp;   // 8 warps <-> 8 values (gate c0..c3, up c0..c3)
-        const int j = j0 + (v & 3);
+    for (int i = tid; i < ng * 128; i += kS1Threads) {
+        const int gi = i >> 7;   // only the slots a group uses hold rows
+        if ((i & 127) < 4 * (s_qs[gi + 1] - s_qs[gi])) {
+            const int r = s_rows[i];
+            if (r < 0 || r >= d) {
+                set_status(status, PROX_ERR_BOUNDS);
+                s_rows[i] = 0;
+            }
+        }
+    }
+    __syncthreads();
+
+    // this warp's quads of the slice
+    const int Q = s_qs[ng];
+    const int qa = static_cast<int>(static_cast<long long>(Q) * warp / kS1Warps);
+    const int qb = static_cast<int>(static_cast<long long>(Q) * (warp + 1) / kS1Warps);
+
+    int gl = 0;
+    while (gl + 1 < ng && s_qs[gl + 1] <= qa) ++gl;
+    auto load_quad = [&](uint32_t (&w)[4][NWC], int q, int g) {
+        const int4 r4 = *reinterpret_cast<const int4*>(s_rows + g * 128 + 4 * (q - s_qs[g]));
+        load_codes<CPL>(w[0], cbase + static_cast<size_t>(r4.x) * F, valid);
+        load_codes<CPL>(w[1], cbase + static_cast<size_t>(r4.y) * F, valid);
+        load_codes<CPL>(w[2], cbase + static_cast<size_t>(r4.z) * F, valid);
+        load_codes<CPL>(w[3], cbase + static_cast<size_t>(r4.w) * F, valid);
+    };
+    int ag[TB][CPL], au[TB][CPL], corr[TB];
+#pragma unroll
+    for (int b = 0; b < TB; ++b) {
+        corr[b] = 0;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) ag[b][c] = au[b][c] = 0;
+    }
+    // multiply one quad: transpose each 4-channel column of the four rows, one dp4a per
+    // channel and projection (gate nibbles as bytes 0..15, up nibbles as 16 * 0..15); at the
+    // end of this warp's part of a group, add the exact integers A = sum((q + 8) qx) -
+    // 8 sum(qx) to the block's per-group sums (integer adds, so their order does not matter)
+    auto step = [&](const uint32_t (&w)[4][NWC], int q, int gcur, int gnext, bool last) {
+        const int qo = q - s_qs[gcur];
 #pragma unroll
         for (int b = 0; b < TB; ++b) {
-            DF t = red[((0 * TB + b) * 8 + v) * 32 + lane];
-            for (int w2 = 1; w2 < kS1Warps; ++w2) t = df_add(t, red[((w2 * TB + b) * 8 + v) * 32 + lane]);
-            if (valid)
-                part[((static_cast<size_t>(s) * TB + b) * F + j) * 2 + (v >> 2)] = make_float2(t.hi, t.lo);
+            const uint32_t q4 = s_qx[(b * gps + gcur) * 32 + qo];
+            corr[b] = dp4a_us(0x08080808u, q4, corr[b]);
+#pragma unroll
+            for (int wcol = 0; wcol < NWC; ++wcol) {
+                const uint32_t w0 = w[0][wcol], w1 = w[1][wcol], w2 = w[2][wcol], w3 = w[3][wcol];
+                const uint32_t a = __byte_perm(w0, w1, 0x5140), bq = __byte_perm(w2, w3, 0x5140);
+                const uint32_t cq = __byte_perm(w0, w1, 0x7362), dq = __byte_perm(w2, w3, 0x7362);
+                const uint32_t t[4] = {__byte_perm(a, bq, 0x5410), __byte_perm(a, bq, 0x7632),
+                                       __byte_perm(cq, dq, 0x5410), __byte_perm(cq, dq, 0x7632)};
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    ag[b][4 * wcol + ch] = dp4a_us(t[ch] & 0x0F0F0F0Fu, q4, ag[b][4 * wcol + ch]);
+                    au[b][4 * wcol + ch] = dp4a_us(t[ch] & 0xF0F0F0F0u, q4, au[b][4 * wcol + ch]);
+                }
+            }
+        }
+        if (last || gnext != gcur) {
+            int* A = s_A + gcur * NV * 32 + lane;
+#pragma unroll
+            for (int b = 0; b < TB; ++b) {
+#pragma unroll
+                for (int ch = 0; ch < CPL; ++ch) {
+                    const int v = (b * CPL + ch) * 2;
+                    atomicAdd(&A[v * 32], ag[b][ch] - corr[b]);
+                    atomicAdd(&A[(v + 1) * 32], (au[b][ch] >> 4) - corr[b]);
+                    ag[b][ch] = au[b][ch] = 0;
+                }
+                corr[b] = 0;
+            }
+        }
+    };
+    uint32_t wa[4][NWC], wb[4][NWC];
+    if (qa < qb) load_quad(wa, qa, gl);
+    for (int q = qa; q < qb; q += 2) {
+        // quad q is in wa; load quad q + 1 into wb, then q + 2 into wa after q is done
+        int g1 = gl;
+        if (q + 1 < qb) {
+            while (g1 + 1 < ng && s_qs[g1 + 1] <= q + 1) ++g1;
+            load_quad(wb, q + 1, g1);
+        }
+        step(wa, q, gl, g1, q + 1 == qb);
+        if (q + 1 >= qb) break;
+        int g2 = g1;
+        if (q + 2 < qb) {
+            while (g2 + 1 < ng && s_qs[g2 + 1] <= q + 2) ++g2;
+            load_quad(wa, q + 2, g2);
+        }
+        step(wb, q + 1, g1, g2, q + 2 == qb);
+        gl = g2;
+    }
+    __syncthreads();
+
+    // per (value, lane): the slice's groups in order, each scaled by sx * sw, summed as a
+    // double-float; then this slice's partial sums go to global memory
+    for (int e = tid; e < NV * 32; e += kS1Threads) {
+        const int v = e >> 5, ln = e & 31;
+        const int b = v / (2 * CPL), ch = (v >> 1) % CPL, proj = v & 1;
+        const int c = tile * TILE + ln * CPL + ch;
+        DF t{0.f, 0.f};
+        if (c < F) {
+            for (int g = 0; g < ng; ++g) {
+                const int A = s_A[(g * NV + v) * 32 + ln];
+                const uint32_t swv = s_sc[g * TILE + ln * CPL + ch];
+                const float sw = __half2float(__ushort_as_half(static_cast<unsigned short>(proj ? swv >> 16 : swv & 0xFFFFu)));
+                t = df_add(t, df_scaled_int(s_sx[b * gps + g], sw, A));
+                int32_t* dbg = proj ? dbg_up : dbg_gate;
+                if (dbg && b < nb) dbg[(static_cast<size_t>(b) * G + g0 + g) * F + c] = A;
+            }
+            part[((static_cast<size_t>(s) * TB + b) * F + c) * 2 + proj] = make_float2(t.hi, t.lo);
         }
     }
     __threadfence();
     __syncthreads();
-    if (tid == 0) last_flag = atomicAdd(&cnt[blk], 1) == S - 1;
+    if (tid == 0) last_flag = atomicAdd(&cnt[tile], 1) == S - 1;
     __syncthreads();
     if (!last_flag) {
         grid_dep_launch();
         return;
     }
     __threadfence();
-    {
-        const int v = warp;
-        const int j = j0 + (v & 3);
-#pragma unroll
-        for (int b = 0; b < TB; ++b) {
-            DF t{0.f, 0.f};
-            if (valid) {
-                for (int s2 = 0; s2 < S; ++s2) {
-                    const float2 p = __ldcg(&part[((static_cast<size_t>(s2) * TB + b) * F + j) * 2 + (v >> 2)]);
-                    t = df_add(t, DF{p.x, p.y});
-                }
+    // last slice of this tile: sum the slices in order, then the salience and its histogram
+    for (int e = tid; e < TB * TILE; e += kS1Threads) {
+        const int b = e / TILE, c = tile * TILE + (e - b * TILE);
+        if (b < nb && c < F) {
+            DF tg{0.f, 0.f}, tu{0.f, 0.f};
+            for (int s2 = 0; s2 < S; ++s2) {
+                const float4 p = __ldcg(reinterpret_cast<const float4*>(part + ((static_cast<size_t>(s2) * TB + b) * F + c) * 2));
+                tg = df_add(tg, DF{p.x, p.y});
+                tu = df_add(tu, DF{p.z, p.w});
             }
-            gu[(b * 8 + v) * 32 + lane] = t.hi + t.lo;
+            const float sg = fabsf(silu_f(tg.hi + tg.lo) * (tu.hi + tu.lo));
+            sigma[static_cast<size_t>(b) * F + c] = sg;
+            atomicAdd(&ghist[b * 2048 + (__float_as_uint(sg) >> 20)], 1);
         }
     }
-    __syncthreads();
-    if (warp < 4 && valid) {
-        const int j = j0 + warp;
-        for (int b = 0; b < nb; ++b) {
-            const float gt = gu[(b * 8 + warp) * 32 + lane];
-            const float ut = gu[(b * 8 + 4 + warp) * 32 + lane];
-            sigma[static_cast<size_t>(b) * F + j] = fabsf(silu_f(gt) * ut);
-        }
-    }
-    if (tid == 0) cnt[blk] = 0;
+    if (tid == 0) cnt[tile] = 0;
     grid_dep_launch();
-}
-
-static int set_smem(const void* fn, size_t bytes) {
-    if (bytes <= 48 * 1024) return PROX_OK;
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(bytes)) == cudaSuccess
-               ? PROX_OK
-               : PROX_ERR_CUDA;
 }
 
 int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, const WsLayout& W,
                        int8_t* dbg_qx, float* dbg_sx, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(d) * 9 + static_cast<size_t>(W.TB) * d;
-    if (set_smem(reinterpret_cast<const void*>(input_quant_kernel), smem) != PROX_OK) return PROX_ERR_CUDA;
-    input_quant_kernel<<<1, kSelThreads, smem, s>>>(
-        x, d, nb, W.TB, k_in, reinterpret_cast<int*>(ws + W.rows),
-        reinterpret_cast<uint32_t*>(ws + W.qxt), reinterpret_cast<float*>(ws + W.sx),
-        reinterpret_cast<int*>(ws + W.gstart), dbg_qx, dbg_sx);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    const size_t smem = static_cast<size_t>(d) * 4 + static_cast<size_t>(W.TB) * d;
+    const int run = select_run(d, kSelThreads);   // d <= 16384: at most 16
+    if (run > 16) return PROX_ERR_UNSUPPORTED;
+    auto fn = run <= 4 ? input_quant_kernel<4> : (run <= 8 ? input_quant_kernel<8> : input_quant_kernel<16>);
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
+    return launch_pdl(fn, dim3(1), dim3(kSelThreads), smem, s, x, d, nb, W.TB, k_in,
+                      reinterpret_cast<int*>(ws + W.grows), reinterpret_cast<int*>(ws + W.gcnt),
+                      reinterpret_cast<int8_t*>(ws + W.gqx), reinterpret_cast<float*>(ws + W.sx),
+                      reinterpret_cast<int*>(ws + W.ghist), dbg_qx, dbg_sx);
 }
 
-template <int TB>
+template <int TB, int CPL>
 static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb,
-                           int S, uint8_t* ws, const WsLayout& W, float* sigma_tile,
+                           const Stage1Plan& pl, uint8_t* ws, const WsLayout& W, float* sigma_tile,
                            int32_t* dbg_gate, int32_t* dbg_up, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(kS1Warps) * TB * 8 * 32 * sizeof(DF);
-    auto fn = stage1_kernel<TB>;
-    if (set_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    fn<<<dim3(W.nblk, S), kS1Threads, smem, s>>>(
-        packed + L.codes_off, reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
-        reinterpret_cast<const int*>(ws + W.rows), reinterpret_cast<const uint32_t*>(ws + W.qxt),
-        reinterpret_cast<const float*>(ws + W.sx), reinterpret_cast<const int*>(ws + W.gstart), S,
-        nb, reinterpret_cast<float2*>(ws + W.s1part), reinterpret_cast<int*>(ws + W.s1_cnt),
-        sigma_tile, dbg_gate, dbg_up, &reinterpret_cast<Control*>(ws + W.control)->status);
-    return cudaGetLastError() == cudaSuccess ? PROX_OK : PROX_ERR_CUDA;
+    constexpr int NV = 2 * CPL * TB;
+    constexpr int TILE = 32 * CPL;
+    const size_t smem = static_cast<size_t>(pl.gps) * NV * 32 * 4 +
+                        static_cast<size_t>(pl.gps) * TILE * 4 + static_cast<size_t>(pl.gps) * 128 * 4 +
+                        static_cast<size_t>(TB) * pl.gps * 128 + static_cast<size_t>(TB) * pl.gps * 4 +
+                        static_cast<size_t>(pl.gps + 1) * 4;
+    auto fn = stage1_kernel<TB, CPL>;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
+    return launch_pdl(fn, dim3(pl.tiles, pl.S), dim3(kS1Threads), smem, s, packed + L.codes_off,
+                      reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
+                      reinterpret_cast<const int*>(ws + W.grows), reinterpret_cast<const int*>(ws + W.gcnt),
+                      reinterpret_cast<const int8_t*>(ws + W.gqx), reinterpret_cast<const float*>(ws + W.sx),
+                      pl.gps, pl.S, nb, reinterpret_cast<float2*>(ws + W.s1part),
+                      reinterpret_cast<int*>(ws + W.s1_cnt), sigma_tile,
+                      reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
+                      &reinterpret_cast<Control*>(ws + W.control)->status);
 }
 
 int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb, int k_in,
                   uint8_t* ws, const WsLayout& W, float* sigma_tile, int32_t* dbg_gate,
                   int32_t* dbg_up, int sms, cudaStream_t s) {
-    const int nrows_est = nb * k_in < d ? nb * k_in : d;
-    int S = stage1_splits(W.nblk, nrows_est, sms);
-    if (S > W.S_max) S = W.S_max;
-    // the narrowest instantiation that holds the tile's tokens
-    if (nb <= 1) return launch_stage1_t<1>(packed, L, d, F, nb, S, ws, W, sigma_tile, dbg_gate, dbg_up, s);
-    if (nb <= 2) return launch_stage1_t<2>(packed, L, d, F, nb, S, ws, W, sigma_tile, dbg_gate, dbg_up, s);
-    return launch_stage1_t<4>(packed, L, d, F, nb, S, ws, W, sigma_tile, dbg_gate, dbg_up, s);
+    (void)k_in;
+    const int TB = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);
+    const Stage1Plan pl = stage1_plan(d, F, TB, sms);
+    if (pl.tiles > W.ntile_max) return PROX_ERR_WORKSPACE;
+    if (TB == 1) return launch_stage1_t<1, 16>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
+    if (TB == 2) return launch_stage1_t<2, 8>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
+    return launch_stage1_t<4, 4>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
 }
 
 }  // namespace prox

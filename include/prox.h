@@ -20,7 +20,7 @@
  *    a status word inside the workspace and reported by prox_get_status.
  *  - Layouts are row-major. bf16 is passed as uint16_t bit patterns.
  *  - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff a multiple of 32 in
- *    [32, 65536]; batch in [1, PROX_MAX_BATCH]. Inputs must be finite.
+ *    [32, 53248]; batch in [1, PROX_MAX_BATCH]. Inputs must be finite.
  *  - Sparsities are fractions in [0, 1). The kept counts are
  *        k    = clamp(floor((1 - sparsity) * d_ff + 0.5), 1, d_ff)
  *        k_in = clamp(floor((1 - input_sparsity) * d_model + 0.5), 1, d_model)
@@ -184,6 +184,11 @@ int prox_get_status(void* ws, void* stream);
 /* Text for an error code (static storage). */
 const char* prox_error_string(int code);
 
+/* The last CUDA failure behind a PROX_ERR_CUDA returned on the calling thread: what the
+ * library was doing and the runtime's error name and text ("none" if there was none).
+ * Thread-local storage, valid until the thread's next failing call. */
+const char* prox_last_cuda_error(void);
+
 /* Test hook: the same input-selection and Stage-1 kernels as prox_build_mask, also storing
  * the exact integer intermediates (technical summary, Stage 1 "Proxy Activation").
  *   qx_out   [batch][d_model] int8: the activation codes (0 on rejected inputs);
@@ -195,6 +200,16 @@ const char* prox_error_string(int code);
 int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double input_sparsity,
                       int8_t* qx_out, float* sx_out, int32_t* acc_gate, int32_t* acc_up,
                       float* salience, void* ws, size_t ws_bytes, void* stream);
+
+/* Test hook for the single-token path whose Stage-2 kernel selects its channels itself
+ * (prox_ffn_forward with one token and no idx_out takes it): runs that path on x [1][d_model]
+ * and also writes every selected channel to sel_out [k] int32 (device): first the channels
+ * above the histogram bin of the k-th salience, in ascending order, then the winners inside
+ * that bin, in ascending order. PROX_ERR_UNSUPPORTED if the shape or sparsity does not take
+ * that path (sparsity 0 is the dense FFN). */
+int prox_debug_fused_forward(const prox_packed* w, const float* x, double sparsity,
+                             double input_sparsity, float* y, int32_t* sel_out, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /* Test hook for the batch path: the ascending union of the rows of idx [batch][k]
  * (device int32) and, per union entry, a bit mask of the tokens that selected it.
