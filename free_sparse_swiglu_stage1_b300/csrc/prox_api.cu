@@ -168,7 +168,7 @@ size_t prox_workspace_bytes(int d_model, int d_ff, int batch) {
 int prox_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (!ws) return PROX_ERR_INVALID_ARG;
     if (!aligned(ws, kAlign)) return PROX_ERR_WORKSPACE;
-    const size_t need = ws_control_bytes((kMaxDff + 127) / 128);
+    const size_t need = ws_control_bytes();
     if (ws_bytes < align_up(sizeof(Control))) return PROX_ERR_WORKSPACE;
     const size_t n = ws_bytes < need ? ws_bytes : need;
     return cuda_ok(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)), "clearing the workspace");

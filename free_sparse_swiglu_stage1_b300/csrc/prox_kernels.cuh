@@ -31,8 +31,10 @@ inline int tile_tokens(int d) { return d <= 4096 ? 4 : (d <= 8192 ? 2 : 1); }
 // Stage 1 work split. A warp reads one kept input row's codes for 32 * CPL channels with
 // one load of CPL bytes per lane (CPL = 16 for one token, 8 for two, 4 for four: the
 // per-token integer sums of a lane's channels stay in registers). A block of 8 warps owns
-// one tile of 32 * CPL channels and a slice of consecutive groups of 128 inputs; all blocks
-// should be resident at once (two per SM).
+// one tile of 32 * CPL channels and a slice of consecutive groups of 128 inputs; the S <= 8
+// slices of a tile form one thread-block cluster, which adds their partial sums through
+// distributed shared memory. All blocks should be resident at once (two per SM).
+constexpr int kStage1MaxSlices = 8;
 struct Stage1Plan {
     int CPL, tiles, S, gps;   // channels per lane, channel tiles, group slices, groups per slice
 };
@@ -43,19 +45,10 @@ inline Stage1Plan stage1_plan(int d, int F, int TB, int sms) {
     pl.tiles = (F + 32 * pl.CPL - 1) / (32 * pl.CPL);
     int S = (2 * sms) / pl.tiles;   // tiles * S <= 2 * sms: one wave
     S = S < 1 ? 1 : (S > G ? G : S);
+    if (S > kStage1MaxSlices) S = kStage1MaxSlices;
     pl.gps = (G + S - 1) / S;
     pl.S = (G + pl.gps - 1) / pl.gps;
     return pl;
-}
-// bytes of Stage-1 partial sums any tile of up to TBmax tokens needs
-inline size_t stage1_part_bytes(int d, int F, int TBmax, int sms) {
-    size_t m = 0;
-    for (int tb = 1; tb <= TBmax; tb <<= 1) {
-        const Stage1Plan pl = stage1_plan(d, F, tb, sms);
-        const size_t b = static_cast<size_t>(pl.S) * tb * F * 16;
-        m = b > m ? b : m;
-    }
-    return m;
 }
 
 // Stage-2 pipeline: one stage = the three rows of one channel (6 d bytes); the number of
@@ -76,9 +69,9 @@ inline int stage2_blocks(int F, int sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, s1_cnt, xbuf, ybuf, grows, gqx, gcnt, sx, ghist, s1part, sigma, idx, ulist,
-        ubits, ypart, total;
-    int TB, P, ntile_max;
+    size_t control, xbuf, ybuf, grows, gqx, gcnt, sx, ghist, sigma, idx, ulist, ubits, ypart,
+        total;
+    int TB, P;
 };
 
 // Workspace of one call shape. Stage-1 inputs are kept per group of 128 inputs: grows [G][128]
@@ -88,12 +81,10 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     WsLayout W;
     const int G = d / 128;
     W.TB = tile_tokens(d);
-    W.ntile_max = (F + 127) / 128;
     W.P = stage2_blocks(F, sms);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     W.control = take(sizeof(Control));
-    W.s1_cnt = take(static_cast<size_t>(W.ntile_max) * 4);
     W.xbuf = take(static_cast<size_t>(B) * d * 4);
     W.ybuf = take(static_cast<size_t>(B) * d * 4);
     W.grows = take(static_cast<size_t>(d) * 4);
@@ -101,7 +92,6 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     W.gcnt = take(static_cast<size_t>(G) * 4);
     W.sx = take(static_cast<size_t>(W.TB) * G * 4);
     W.ghist = take(static_cast<size_t>(W.TB) * 2048 * 4);
-    W.s1part = take(stage1_part_bytes(d, F, W.TB, sms));
     W.sigma = take(static_cast<size_t>(B) * F * 4);
     W.idx = take(static_cast<size_t>(B) * F * 4);
     W.ulist = take(static_cast<size_t>(F) * 4);
@@ -111,8 +101,8 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     return W;
 }
 
-// Bytes of the control region that prox_workspace_init clears (control block + counters).
-inline size_t ws_control_bytes(int ntile) { return align_up(sizeof(Control)) + align_up(ntile * 4); }
+// Bytes of the control region that prox_workspace_init clears.
+inline size_t ws_control_bytes() { return align_up(sizeof(Control)); }
 
 // ------------------------------------------------------------------ launches
 // Records a failed CUDA call (the error and what was being done) for prox_last_cuda_error;

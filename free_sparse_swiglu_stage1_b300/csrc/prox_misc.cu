@@ -44,6 +44,7 @@ rmsnorm_kernel(const float* __restrict__ y, float* __restrict__ x_out, int d, fl
     const float* yr = y + static_cast<size_t>(blockIdx.x) * d;
     float* xr = x_out + static_cast<size_t>(blockIdx.x) * d;
     grid_dep_wait();
+    grid_dep_launch();
     float s = 0.f;
     for (int i = threadIdx.x; i < d; i += 256) s = fmaf(yr[i], yr[i], s);
 #pragma unroll
@@ -58,7 +59,6 @@ rmsnorm_kernel(const float* __restrict__ y, float* __restrict__ x_out, int d, fl
     __syncthreads();
     const float r = scale;
     for (int i = threadIdx.x; i < d; i += 256) xr[i] = yr[i] / r;
-    grid_dep_launch();
 }
 
 __global__ void iota_kernel(int32_t* __restrict__ out, int n, int rows) {

@@ -34,6 +34,7 @@ topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__
     }
     __syncthreads();
     grid_dep_wait();
+    grid_dep_launch();
     // the token's salience row and its first-pass histogram, each one bulk copy
     if (tid == 0) {
         mbar_arrive_expect_tx(&bar, static_cast<uint32_t>(F) * 4 + 2048 * 4);
@@ -51,23 +52,27 @@ topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__
     uint64_t mine;
     const int cnt = block_take_topk<NT, RUN>(keys, F, T, take, eq_total, wsum, mine);
     int total;
-    int pos = block_exclusive_scan<NT>(cnt, wsum, total);
-    int32_t* out = idx + static_cast<size_t>(b) * k;
+    int pos = block_exclusive_scan<NT>(cnt, wsum, total);   // ends with a barrier: keys are free
+    // the mask is assembled in shared memory (over the keys) and written out coalesced
+    int32_t* s_idx = reinterpret_cast<int32_t*>(keys);
     const int lo = tid * RUN;
 #pragma unroll
     for (int i = 0; i < RUN; ++i)
-        if (((mine >> i) & 1ull) && pos < k) out[pos++] = lo + i;
-    grid_dep_launch();
+        if (((mine >> i) & 1ull) && pos < k) s_idx[pos++] = lo + i;
+    __syncthreads();
+    int32_t* out = idx + static_cast<size_t>(b) * k;
+    for (int i = tid; i < k; i += NT) out[i] = s_idx[i];
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
 union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __restrict__ ulist,
              uint32_t* __restrict__ ubits, int* __restrict__ count, int* __restrict__ status) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     uint32_t* bits = reinterpret_cast<uint32_t*>(smem);
     __shared__ int wsum[kTopkThreads / 32 + 4];
     const int tid = threadIdx.x;
     grid_dep_wait();
+    grid_dep_launch();
     for (int i = tid; i < F; i += kTopkThreads) bits[i] = 0u;
     __syncthreads();
     for (int b = 0; b < nb; ++b)
@@ -93,7 +98,6 @@ union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __r
         }
     }
     if (tid == 0) *count = total;
-    grid_dep_launch();
 }
 
 template <int NT, int RUN>

@@ -26,6 +26,8 @@
 //   block to finish a channel tile does the final sum and the salience), so the result is
 //   deterministic. That block also counts the salience's top 11 bits into a histogram the
 //   top-k starts from.
+#include <cooperative_groups.h>
+
 #include "prox_kernels.cuh"
 
 namespace prox {
@@ -57,8 +59,10 @@ input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
     const int g_mine = lo >> 7;
     const bool active = lo < hi;
     const int gl = tid & (tpg - 1);                // this thread's place among its group's
+    const int TBs = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);   // tokens the Stage-1 kernel reads
 
     grid_dep_wait();
+    grid_dep_launch();
     for (int i = tid; i < TB * 512; i += NT)   // filled by Stage 1 for the top-k
         reinterpret_cast<int4*>(ghist)[i] = make_int4(0, 0, 0, 0);
     uint64_t any = 0ull;
@@ -140,7 +144,7 @@ input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
             if ((any >> e) & 1ull) {
                 const int i = lo + e;
                 rows_g[p] = i;
-                for (int b = 0; b < TB; ++b)
+                for (int b = 0; b < TBs; ++b)
                     gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + p] = b < nb ? qx8[b * d + i] : 0;
                 ++p;
             }
@@ -149,12 +153,11 @@ input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
             const int padded = (n_g + 3) & ~3;
             for (int q = n_g; q < padded; ++q) {
                 rows_g[q] = last;
-                for (int b = 0; b < TB; ++b) gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + q] = 0;
+                for (int b = 0; b < TBs; ++b) gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + q] = 0;
             }
             gcnt[g_mine] = padded;
         }
     }
-    grid_dep_launch();
 }
 
 // dp4a with unsigned bytes in a and signed bytes in b
@@ -183,8 +186,8 @@ __global__ void __launch_bounds__(kS1Threads, 2)
 stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ scales, int d, int F,
               const int* __restrict__ grows, const int* __restrict__ gcnt,
               const int8_t* __restrict__ gqx, const float* __restrict__ sx, int gps, int S,
-              int nb, float2* __restrict__ part, int* __restrict__ cnt, float* __restrict__ sigma,
-              int* __restrict__ ghist, int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up,
+              int nb, float* __restrict__ sigma, int* __restrict__ ghist,
+              int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up,
               int* __restrict__ status) {
     constexpr int NV = 2 * CPL * TB;       // values per lane: (token, channel, projection)
     constexpr int NWC = CPL / 4;           // code words per lane and row
@@ -196,7 +199,7 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     uint32_t* s_qx = reinterpret_cast<uint32_t*>(s_rows + gps * 128);      // [TB][gps][32]
     float* s_sx = reinterpret_cast<float*>(s_qx + TB * gps * 32);          // [TB][gps]
     int* s_qs = reinterpret_cast<int*>(s_sx + TB * gps);                   // [gps + 1] quad starts
-    __shared__ int last_flag;
+    __shared__ DF s_part[NV * 32];   // this slice's double-float sums, read by the whole cluster
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x, s = blockIdx.y;
     const int G = d >> 7;
@@ -216,6 +219,7 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     for (int i = tid; i < ng * NV * 32 / 4; i += kS1Threads)
         reinterpret_cast<int4*>(s_A)[i] = make_int4(0, 0, 0, 0);
     grid_dep_wait();
+    grid_dep_launch();
     for (int i = tid; i < ng * 32; i += kS1Threads)
         reinterpret_cast<int4*>(s_rows)[i] = __ldcg(reinterpret_cast<const int4*>(grows + g0 * 128) + i);
     for (int i = tid; i < TB * ng * 32; i += kS1Threads) {
@@ -350,50 +354,62 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     __syncthreads();
 
     // per (value, lane): the slice's groups in order, each scaled by sx * sw, summed as a
-    // double-float; then this slice's partial sums go to global memory
-    for (int e = tid; e < NV * 32; e += kS1Threads) {
-        const int v = e >> 5, ln = e & 31;
-        const int b = v / (2 * CPL), ch = (v >> 1) % CPL, proj = v & 1;
-        const int c = tile * TILE + ln * CPL + ch;
-        DF t{0.f, 0.f};
-        if (c < F) {
-            for (int g = 0; g < ng; ++g) {
-                const int A = s_A[(g * NV + v) * 32 + ln];
-                const uint32_t swv = s_sc[g * TILE + ln * CPL + ch];
-                const float sw = __half2float(__ushort_as_half(static_cast<unsigned short>(proj ? swv >> 16 : swv & 0xFFFFu)));
-                t = df_add(t, df_scaled_int(s_sx[b * gps + g], sw, A));
-                int32_t* dbg = proj ? dbg_up : dbg_gate;
-                if (dbg && b < nb) dbg[(static_cast<size_t>(b) * G + g0 + g) * F + c] = A;
-            }
-            part[((static_cast<size_t>(s) * TB + b) * F + c) * 2 + proj] = make_float2(t.hi, t.lo);
+    // double-float; then this slice's partial sums go to global memory. Each thread carries
+    // its NV * 32 / 256 entries side by side, so their dependent chains overlap.
+    constexpr int EPT = NV * 32 / kS1Threads;   // 4
+    DF t[EPT];
+    int ve[EPT], lne[EPT];
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        const int e = tid + k * kS1Threads;
+        ve[k] = e >> 5;
+        lne[k] = e & 31;
+        t[k] = DF{0.f, 0.f};
+    }
+    for (int g = 0; g < ng; ++g) {
+#pragma unroll
+        for (int k = 0; k < EPT; ++k) {
+            const int v = ve[k], ln = lne[k];
+            const int b = v / (2 * CPL), ch = (v >> 1) % CPL, proj = v & 1;
+            const int A = s_A[(g * NV + v) * 32 + ln];
+            const uint32_t swv = s_sc[g * TILE + ln * CPL + ch];
+            const float sw = __half2float(__ushort_as_half(static_cast<unsigned short>(proj ? swv >> 16 : swv & 0xFFFFu)));
+            t[k] = df_add(t[k], df_scaled_int(s_sx[b * gps + g], sw, A));
+            int32_t* dbg = proj ? dbg_up : dbg_gate;
+            const int c = tile * TILE + ln * CPL + ch;
+            if (dbg && b < nb && c < F) dbg[(static_cast<size_t>(b) * G + g0 + g) * F + c] = A;
         }
     }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) last_flag = atomicAdd(&cnt[tile], 1) == S - 1;
-    __syncthreads();
-    if (!last_flag) {
-        grid_dep_launch();
-        return;
-    }
-    __threadfence();
-    // last slice of this tile: sum the slices in order, then the salience and its histogram
-    for (int e = tid; e < TB * TILE; e += kS1Threads) {
-        const int b = e / TILE, c = tile * TILE + (e - b * TILE);
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) s_part[tid + k * kS1Threads] = t[k];
+
+    // the S slices of this tile are one cluster: after the cluster barrier, rank r adds the
+    // slices' sums in order for its share of the tile's (token, channel) pairs, through
+    // distributed shared memory, and writes their salience and histogram counts
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int npairs = TB * TILE;
+    const int r = static_cast<int>(cluster.block_rank());
+    const int pa = npairs * r / S, pb = npairs * (r + 1) / S;
+    for (int pr = pa + tid; pr < pb; pr += kS1Threads) {
+        const int b = pr / TILE, cl = pr - b * TILE;
+        const int c = tile * TILE + cl;
+        const int ln = cl / CPL, ch = cl - ln * CPL;
+        const int eg = ((b * CPL + ch) * 2) * 32 + ln;   // gate entry; up entry is eg + 32
         if (b < nb && c < F) {
             DF tg{0.f, 0.f}, tu{0.f, 0.f};
             for (int s2 = 0; s2 < S; ++s2) {
-                const float4 p = __ldcg(reinterpret_cast<const float4*>(part + ((static_cast<size_t>(s2) * TB + b) * F + c) * 2));
-                tg = df_add(tg, DF{p.x, p.y});
-                tu = df_add(tu, DF{p.z, p.w});
+                const DF* rp = cluster.map_shared_rank(s_part, s2);
+                tg = df_add(tg, rp[eg]);
+                tu = df_add(tu, rp[eg + 32]);
             }
             const float sg = fabsf(silu_f(tg.hi + tg.lo) * (tu.hi + tu.lo));
             sigma[static_cast<size_t>(b) * F + c] = sg;
             atomicAdd(&ghist[b * 2048 + (__float_as_uint(sg) >> 20)], 1);
         }
     }
-    if (tid == 0) cnt[tile] = 0;
-    grid_dep_launch();
+    cluster.sync();   // no block leaves while another still reads its shared memory
 }
 
 int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, const WsLayout& W,
@@ -421,14 +437,29 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
                         static_cast<size_t>(pl.gps + 1) * 4;
     auto fn = stage1_kernel<TB, CPL>;
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    return launch_pdl(fn, dim3(pl.tiles, pl.S), dim3(kS1Threads), smem, s, packed + L.codes_off,
-                      reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
-                      reinterpret_cast<const int*>(ws + W.grows), reinterpret_cast<const int*>(ws + W.gcnt),
-                      reinterpret_cast<const int8_t*>(ws + W.gqx), reinterpret_cast<const float*>(ws + W.sx),
-                      pl.gps, pl.S, nb, reinterpret_cast<float2*>(ws + W.s1part),
-                      reinterpret_cast<int*>(ws + W.s1_cnt), sigma_tile,
-                      reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
-                      &reinterpret_cast<Control*>(ws + W.control)->status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.tiles, pl.S);
+    cfg.blockDim = dim3(kS1Threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;   // the S slices of a tile
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = pl.S;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t err = cudaLaunchKernelEx(
+        &cfg, fn, packed + L.codes_off, reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
+        static_cast<const int*>(reinterpret_cast<const int*>(ws + W.grows)),
+        static_cast<const int*>(reinterpret_cast<const int*>(ws + W.gcnt)),
+        static_cast<const int8_t*>(reinterpret_cast<const int8_t*>(ws + W.gqx)),
+        static_cast<const float*>(reinterpret_cast<const float*>(ws + W.sx)), pl.gps, pl.S, nb,
+        sigma_tile, reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
+        &reinterpret_cast<Control*>(ws + W.control)->status);
+    return err == cudaSuccess ? PROX_OK : cuda_fail(err, "Stage-1 cluster launch");
 }
 
 int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb, int k_in,
@@ -437,7 +468,6 @@ int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, in
     (void)k_in;
     const int TB = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);
     const Stage1Plan pl = stage1_plan(d, F, TB, sms);
-    if (pl.tiles > W.ntile_max) return PROX_ERR_WORKSPACE;
     if (TB == 1) return launch_stage1_t<1, 16>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
     if (TB == 2) return launch_stage1_t<2, 8>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
     return launch_stage1_t<4, 4>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);

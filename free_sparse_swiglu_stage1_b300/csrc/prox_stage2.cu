@@ -288,6 +288,7 @@ stage2_kernel(const uint16_t* __restrict__ rows, int d, int F, const float* __re
         mbar_init_fence();
     }
     grid_dep_wait();   // the channel list (or the salience), the activations: earlier kernels
+    grid_dep_launch();
 
     // Group gi consumes channels gi, gi + NG, ...; since NG divides the ring size, its
     // channels always land in its own ring slots, and its leader refills a slot as soon as the
@@ -469,7 +470,6 @@ stage2_kernel(const uint16_t* __restrict__ rows, int d, int F, const float* __re
             reinterpret_cast<float4*>(yp)[i] = t;
         }
     }
-    grid_dep_launch();
 }
 
 // y[b][:] = sum over blocks p (fixed order) of ypart[p][b][:]. A block covers 8 float4
@@ -482,6 +482,7 @@ reduce_kernel(const float4* __restrict__ ypart, int P, int TB, int d, float4* __
     const int col = blockIdx.x * 8 + cx;
     const int b = blockIdx.y;
     grid_dep_wait();
+    grid_dep_launch();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < n4) {
         for (int p = pg; p < P; p += 32) {
@@ -499,7 +500,6 @@ reduce_kernel(const float4* __restrict__ ypart, int P, int TB, int d, float4* __
         }
         y[static_cast<size_t>(b) * n4 + col] = t;
     }
-    grid_dep_launch();
 }
 
 // Consumer layout of the Stage-2 kernel for a row length and token tile: NG groups of WPG
