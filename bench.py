@@ -175,10 +175,11 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def source_hash() -> str:
+def source_hash(names=None) -> str:
+    """Hash of the CUDA sources `names` (file names under csrc/; all of them by default)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "free_sparse_swiglu_stage1_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(names or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -187,14 +188,15 @@ def source_hash() -> str:
 
 def profiled_traffic(kernel: str) -> tuple[float | None, str | None]:
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current sources."""
+    the current sources of that kernel (its translation unit and the headers it includes,
+    listed in the record)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel)
     except (OSError, ValueError):
         return None, None
-    if not rec or rec.get("source_hash") != source_hash():
+    if not rec or rec.get("source_hash") != source_hash(rec.get("sources")):
         return None, None
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 

@@ -69,14 +69,15 @@ inline int stage2_blocks(int F, int sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, xbuf, ybuf, grows, gqx, gcnt, sx, ghist, sigma, idx, ulist, ubits, ypart,
+    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, sigma, idx, ulist, ubits, ypart,
         total;
     int TB, P;
 };
 
 // Workspace of one call shape. Stage-1 inputs are kept per group of 128 inputs: grows [G][128]
 // (the group's kept inputs, ascending, padded to a multiple of 4 with copies of the last),
-// gcnt [G] (padded counts), gqx [TB][G][128] int8 codes, sx [TB][G] scales.
+// gcnt [G] (padded counts), gq [G + 1] (quad offsets: exclusive sums of gcnt / 4),
+// gqx [TB][G][128] int8 codes, sx [TB][G] scales.
 inline WsLayout ws_layout(int d, int F, int B, int sms) {
     WsLayout W;
     const int G = d / 128;
@@ -90,6 +91,7 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     W.grows = take(static_cast<size_t>(d) * 4);
     W.gqx = take(static_cast<size_t>(W.TB) * d);
     W.gcnt = take(static_cast<size_t>(G) * 4);
+    W.gq = take(static_cast<size_t>(G + 1) * 4);
     W.sx = take(static_cast<size_t>(W.TB) * G * 4);
     W.ghist = take(static_cast<size_t>(W.TB) * 2048 * 4);
     W.sigma = take(static_cast<size_t>(B) * F * 4);

@@ -41,9 +41,8 @@ topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__
         bulk_g2s(keys, sigma + static_cast<size_t>(b) * F, static_cast<uint32_t>(F) * 4, &bar);
         bulk_g2s(hist, ghist + static_cast<size_t>(b) * 2048, 2048 * 4, &bar);
     }
-    if (!mbar_wait(&bar, 0u, spin, status)) {
+    if (!__syncthreads_and(mbar_wait(&bar, 0u, spin, status))) {
         // nothing usable arrived: leave the mask unwritten; the status word says why
-        // (every thread waits on the same barrier, so all of them leave here together)
         return;
     }
     uint32_t T;

@@ -39,18 +39,20 @@ constexpr int kS1Warps = kS1Threads / 32;
 // Input selection and activation codes for one tile of nb tokens (see the file comment).
 // Thread t owns the run of inputs [t*RUN, t*RUN + RUN), RUN a power of two in [4, 16], so a
 // run lies inside one group of 128 and a group's runs are 128/RUN aligned lanes of one warp.
-// Outputs: grows [G][128], gcnt [G], gqx [TB][G][128], sx [TB][G]; clears ghist [TB][2048].
+// Outputs: grows [G][128], gcnt [G], gq [G + 1], gqx [TB][G][128], sx [TB][G]; clears
+// ghist [TB][2048].
 template <int RUN>
 __global__ void __launch_bounds__(kSelThreads)
 input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
-                   int* __restrict__ grows, int* __restrict__ gcnt, int8_t* __restrict__ gqx,
-                   float* __restrict__ sx_ws, int* __restrict__ ghist,
+                   int* __restrict__ grows, int* __restrict__ gcnt, int* __restrict__ gq,
+                   int8_t* __restrict__ gqx, float* __restrict__ sx_ws, int* __restrict__ ghist,
                    int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                 // [d]
     int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);                   // [TB][d]
     __shared__ int hist[2 * 2048];
     __shared__ int wsum[kSelThreads / 32 + 4];
+    __shared__ int s_gq[128];   // quads per group
     constexpr int NT = kSelThreads;
     constexpr int tpg = 128 / RUN;                 // threads per group (8 .. 32)
     const int tid = threadIdx.x;
@@ -156,7 +158,33 @@ input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
                 for (int b = 0; b < TBs; ++b) gqx[(static_cast<size_t>(b) * G + g_mine) * 128 + q] = 0;
             }
             gcnt[g_mine] = padded;
+            s_gq[g_mine] = padded >> 2;
         }
+    }
+    // quad offsets of the groups (exclusive sums of the padded counts / 4), for Stage 1
+    __syncthreads();
+    if (tid < 32) {
+        int c4v[4], loc = 0;
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int g = tid * 4 + m4;
+            c4v[m4] = g < G ? s_gq[g] : 0;
+            loc += c4v[m4];
+        }
+        int incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += y;
+        }
+        int run = incl - loc;
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int g = tid * 4 + m4;
+            if (g < G) gq[g] = run;
+            run += c4v[m4];
+        }
+        if (tid == 31) gq[G] = incl;
     }
 }
 
@@ -184,7 +212,7 @@ __device__ __forceinline__ void load_codes(uint32_t (&w)[CPL / 4], const uint8_t
 template <int TB, int CPL>
 __global__ void __launch_bounds__(kS1Threads, 2)
 stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ scales, int d, int F,
-              const int* __restrict__ grows, const int* __restrict__ gcnt,
+              const int* __restrict__ grows, const int* __restrict__ gq,
               const int8_t* __restrict__ gqx, const float* __restrict__ sx, int gps, int S,
               int nb, float* __restrict__ sigma, int* __restrict__ ghist,
               int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up,
@@ -230,48 +258,23 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
         const int b = i / ng, gl = i - b * ng;
         s_sx[b * gps + gl] = __ldcg(sx + b * G + g0 + gl);
     }
-    if (tid < 32) {
-        // quad starts of the slice's groups: exclusive scan of gcnt / 4, 4 groups per lane
-        int c4v[4], loc = 0;
-#pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-            const int gl = lane * 4 + m4;
-            int c = gl < ng ? __ldcg(gcnt + g0 + gl) : 0;
-            if (c < 0 || c > 128 || (c & 3)) {
-                set_status(status, PROX_ERR_BOUNDS);
-                c = 0;
-            }
-            c4v[m4] = c >> 2;
-            loc += c4v[m4];
-        }
-        int incl = loc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        int run = incl - loc;
-#pragma unroll
-        for (int m4 = 0; m4 < 4; ++m4) {
-            const int gl = lane * 4 + m4;
-            if (gl < ng) s_qs[gl] = run;
-            run += c4v[m4];
-        }
-        if (lane == 31) s_qs[ng] = incl;
+    for (int i = tid; i <= ng; i += kS1Threads) s_qs[i] = __ldcg(gq + g0 + i);
+    __syncthreads();
+    // quad starts relative to the slice; a group holds at most 32 quads
+    int qv = 0, qprev = 0;
+    if (tid <= ng) {
+        qv = s_qs[tid] - s_qs[0];
+        qprev = tid > 0 ? s_qs[tid - 1] - s_qs[0] : 0;
     }
     __syncthreads();
-    for (int i = tid; i < ng * 128; i += kS1Threads) {
-        const int gi = i >> 7;   // only the slots a group uses hold rows
-        if ((i & 127) < 4 * (s_qs[gi + 1] - s_qs[gi])) {
-            const int r = s_rows[i];
-            if (r < 0 || r >= d) {
-                set_status(status, PROX_ERR_BOUNDS);
-                s_rows[i] = 0;
-            }
+    if (tid <= ng) {
+        if (qv < qprev || qv - qprev > 32 || qv > 32 * tid) {
+            set_status(status, PROX_ERR_BOUNDS);
+            qv = qprev;
         }
+        s_qs[tid] = qv;
     }
     __syncthreads();
-
     // this warp's quads of the slice
     const int Q = s_qs[ng];
     const int qa = static_cast<int>(static_cast<long long>(Q) * warp / kS1Warps);
@@ -280,7 +283,12 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     int gl = 0;
     while (gl + 1 < ng && s_qs[gl + 1] <= qa) ++gl;
     auto load_quad = [&](uint32_t (&w)[4][NWC], int q, int g) {
-        const int4 r4 = *reinterpret_cast<const int4*>(s_rows + g * 128 + 4 * (q - s_qs[g]));
+        int4 r4 = *reinterpret_cast<const int4*>(s_rows + g * 128 + 4 * (q - s_qs[g]));
+        if (static_cast<unsigned>(r4.x) >= static_cast<unsigned>(d) || static_cast<unsigned>(r4.y) >= static_cast<unsigned>(d) ||
+            static_cast<unsigned>(r4.z) >= static_cast<unsigned>(d) || static_cast<unsigned>(r4.w) >= static_cast<unsigned>(d)) {
+            set_status(status, PROX_ERR_BOUNDS);   // a row outside the layer: read row 0 instead
+            r4 = make_int4(0, 0, 0, 0);
+        }
         load_codes<CPL>(w[0], cbase + static_cast<size_t>(r4.x) * F, valid);
         load_codes<CPL>(w[1], cbase + static_cast<size_t>(r4.y) * F, valid);
         load_codes<CPL>(w[2], cbase + static_cast<size_t>(r4.z) * F, valid);
@@ -421,7 +429,8 @@ int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, con
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
     return launch_pdl(fn, dim3(1), dim3(kSelThreads), smem, s, x, d, nb, W.TB, k_in,
                       reinterpret_cast<int*>(ws + W.grows), reinterpret_cast<int*>(ws + W.gcnt),
-                      reinterpret_cast<int8_t*>(ws + W.gqx), reinterpret_cast<float*>(ws + W.sx),
+                      reinterpret_cast<int*>(ws + W.gq), reinterpret_cast<int8_t*>(ws + W.gqx),
+                      reinterpret_cast<float*>(ws + W.sx),
                       reinterpret_cast<int*>(ws + W.ghist), dbg_qx, dbg_sx);
 }
 
@@ -454,7 +463,7 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
     const cudaError_t err = cudaLaunchKernelEx(
         &cfg, fn, packed + L.codes_off, reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
         static_cast<const int*>(reinterpret_cast<const int*>(ws + W.grows)),
-        static_cast<const int*>(reinterpret_cast<const int*>(ws + W.gcnt)),
+        static_cast<const int*>(reinterpret_cast<const int*>(ws + W.gq)),
         static_cast<const int8_t*>(reinterpret_cast<const int8_t*>(ws + W.gqx)),
         static_cast<const float*>(reinterpret_cast<const float*>(ws + W.sx)), pl.gps, pl.S, nb,
         sigma_tile, reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,

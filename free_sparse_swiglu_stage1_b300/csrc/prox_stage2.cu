@@ -137,6 +137,7 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
 template <int KRUN, typename Start>
 __device__ int select_channels(const float* __restrict__ sigma, const int* __restrict__ ghist, int F,
                                int k, int* s_list, uint32_t* s_bits, int* hist, int* wsum,
+                               unsigned char* scratch, uint64_t* bar, long long spin,
                                int* status, int32_t* dbg_sel, Start start) {
     constexpr int NT = kS2MaxConsumers;
     constexpr int NW = NT / 32;
@@ -144,23 +145,32 @@ __device__ int select_channels(const float* __restrict__ sigma, const int* __res
     const int P = gridDim.x, blk = blockIdx.x;
     int* sel = wsum + NW;
     int* s_cnt = sel + 3;
-    // 1. the bin of the k-th largest key
-    for (int i = tid; i < 2048; i += NT) hist[i] = __ldcg(ghist + i);
+    // 1. the salience row (into the not yet used stage memory) and the first-pass histogram,
+    //    one bulk copy each, then the bin of the k-th largest key
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(F) * 4 + 2048 * 4);
+        bulk_g2s(scratch, sigma, static_cast<uint32_t>(F) * 4, bar);
+        bulk_g2s(hist, ghist, 2048 * 4, bar);
+    }
     for (int i = tid; i < 2048; i += NT) hist[2048 + i] = 0;
     const int lo = tid * KRUN;
     const int nv = lo < F ? (F - lo < KRUN ? F - lo : KRUN) : 0;
+    // every thread decides the same way (a wait can run out for some threads only)
+    if (!__syncthreads_and(mbar_wait(bar, 0u, spin, status))) {
+        // nothing usable arrived (the status word says why): this block takes no channels
+        return 0;
+    }
     uint32_t key[KRUN];
 #pragma unroll
     for (int i4 = 0; i4 < KRUN / 4; ++i4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (4 * i4 < nv) v = __ldcg(reinterpret_cast<const float4*>(sigma + lo + 4 * i4));
-        key[4 * i4] = __float_as_uint(v.x) & 0x7fffffffu;
-        key[4 * i4 + 1] = __float_as_uint(v.y) & 0x7fffffffu;
-        key[4 * i4 + 2] = __float_as_uint(v.z) & 0x7fffffffu;
-        key[4 * i4 + 3] = __float_as_uint(v.w) & 0x7fffffffu;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (4 * i4 < nv) v = *reinterpret_cast<const uint4*>(scratch + 4 * (lo + 4 * i4));
+        key[4 * i4] = v.x & 0x7fffffffu;
+        key[4 * i4 + 1] = v.y & 0x7fffffffu;
+        key[4 * i4 + 2] = v.z & 0x7fffffffu;
+        key[4 * i4 + 3] = v.w & 0x7fffffffu;
     }
-    __syncthreads();
-    block_find_bin<NT>(hist, 2048, k, wsum, sel);
+    block_find_bin<NT>(hist, 2048, k, wsum, sel);   // its barriers also free the stage memory
     const uint32_t b1 = static_cast<uint32_t>(sel[0]);
     const int above = sel[1];
     // sure channels: bins above b1
@@ -280,13 +290,16 @@ stage2_kernel(const uint16_t* __restrict__ rows, int d, int F, const float* __re
     float* red = reinterpret_cast<float*>(s_bits + kStage2ListMax);    // [NG][2][V][WPG]
     int* s_hist = reinterpret_cast<int*>(red + NG * 2 * V * WPG);     // [2][2048] (select mode)
     int* s_wsum = s_hist + (KRUN ? 2 * 2048 : 0);                      // [NW + 4]
+    uint64_t* s_selbar = reinterpret_cast<uint64_t*>(s_wsum + (KRUN ? NW + 4 : 0));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = gridDim.x;
 
     if (tid == 0) {
         for (int i = 0; i < nstage; ++i) mbar_init(&full[i], 1);
+        if (KRUN > 0) mbar_init(s_selbar, 1);
         mbar_init_fence();
     }
+    __syncthreads();
     grid_dep_wait();   // the channel list (or the salience), the activations: earlier kernels
     grid_dep_launch();
 
@@ -305,8 +318,8 @@ stage2_kernel(const uint16_t* __restrict__ rows, int d, int F, const float* __re
 
     int nloc;
     if constexpr (KRUN > 0) {
-        nloc = select_channels<KRUN>(sigma, ghist, F, ksel, s_list, s_bits, s_hist, s_wsum, status,
-                                     dbg_sel, [&](int nsure) {
+        nloc = select_channels<KRUN>(sigma, ghist, F, ksel, s_list, s_bits, s_hist, s_wsum, stages,
+                                     s_selbar, spin, status, dbg_sel, [&](int nsure) {
                                          // copies of the sure channels start before the
                                          // boundary bin is resolved
                                          if (leader)
@@ -527,7 +540,7 @@ static size_t stage2_smem_bytes(int d, int TB, const S2Shape& sh, bool select) {
     return static_cast<size_t>(nstage) * 6 * d + nstage * sizeof(uint64_t) +
            2 * kStage2ListMax * sizeof(int) +
            static_cast<size_t>(sh.NG) * 2 * 2 * TB * sh.WPG * sizeof(float) +
-           (select ? (2 * 2048 + NW + 4) * sizeof(int) : 0);
+           (select ? (2 * 2048 + NW + 4) * sizeof(int) + 2 * sizeof(uint64_t) : 0);
 }
 
 template <int TB, int CPT, int KRUN>

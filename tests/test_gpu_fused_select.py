@@ -1,12 +1,12 @@
 """The single-token Stage-2 variant that selects its own channels.
 
-This variant folds the top-k into the front of the Stage-2 kernel: every block finds, from
-Stage 1's salience histogram, the bin of the k-th value, starts on the channels above it, and
-resolves the winners inside that bin while the first copies are in flight. It is reached
-through the prox_debug_fused_forward hook. The selected set must be exactly the mask
-prox_build_mask returns (the same ranking rule on the same salience), the output must agree
-with the two-step path (mask, then Stage 2 over it) and with the oracle, and ties must go to
-the lower channel index.
+This variant folds the top-k into the front of the Stage-2 kernel: every block bulk-loads the
+salience and Stage 1's histogram of it, finds the bin of the k-th value, starts copying the
+channels above that bin, and resolves the winners inside the bin while those copies are in
+flight. It is reached through the prox_debug_fused_forward hook, which also returns the
+selected channels. The selected set must be exactly the mask prox_build_mask returns (the same
+ranking rule on the same salience), the output must agree with the two-step path (mask, then
+Stage 2 over it) and with the oracle, and ties must go to the lower channel index.
 """
 import numpy as np
 import pytest
