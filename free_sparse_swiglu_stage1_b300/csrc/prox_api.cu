@@ -88,6 +88,27 @@ int run_stage2_tile(const prox_packed* w, const PackedLayout& L, const float* xt
                          sms, s);
 }
 
+// Stage 2 of a whole batch on the tensor cores: one pass over the union of every token's mask
+// (idx == nullptr: every channel).
+int run_stage2_tc(const prox_packed* w, const PackedLayout& L, const float* x, int B,
+                  const int32_t* idx, int k, float* y, uint8_t* ws, const WsLayout& W, int sms,
+                  cudaStream_t s) {
+    const int d = w->d_model, F = w->d_ff;
+    const uint8_t* packed = static_cast<const uint8_t*>(w->base);
+    if (!idx)
+        return launch_stage2_tc(packed, L, d, F, x, B, nullptr, nullptr, nullptr, F, y, ws, W, sms, s);
+    Control* ctrl = reinterpret_cast<Control*>(ws + W.control);
+    int32_t* ulist = reinterpret_cast<int32_t*>(ws + W.ulist);
+    uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
+    PROX_TRY(launch_union(idx, B, k, F, ulist, ubits, &ctrl->union_count, &ctrl->status, s));
+    return launch_stage2_tc(packed, L, d, F, x, B, ulist, ubits, &ctrl->union_count, 0, y, ws, W,
+                            sms, s);
+}
+
+bool use_tc(const prox_packed* w, int B, const WsLayout& W, int sms) {
+    return W.BPtc >= B && stage2_tc_supported(w->d_model, w->d_ff, B, sms);
+}
+
 struct Debug {
     int8_t* qx = nullptr;
     float* sx = nullptr;
@@ -111,6 +132,8 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
     const bool all_channels = (k == F) && !dbg;
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + W.idx);
     float* sigma = (dbg && dbg->salience) ? dbg->salience : reinterpret_cast<float*>(ws + W.sigma);
+    // a large batch makes every tile's mask first, then one tensor-core Stage 2 over them all
+    const bool tc = y && !dbg && use_tc(w, B, W, sms);
     for (int t0 = 0; t0 < B; t0 += W.TB) {
         const int nb = B - t0 < W.TB ? B - t0 : W.TB;
         const float* xt = x + static_cast<size_t>(t0) * d;
@@ -118,7 +141,7 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
         if (all_channels) {
             // sparsity 0: every channel is kept, the ranking cannot change the result
             if (idx_out) PROX_TRY(launch_iota(idx_t, F, nb, s));
-            if (y)
+            if (y && !tc)
                 PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, true,
                                          y + static_cast<size_t>(t0) * d, ws, W, sms, s));
             continue;
@@ -142,10 +165,11 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
         PROX_TRY(launch_topk(sigma + static_cast<size_t>(t0) * F, F, nb, k, idx_t,
                              reinterpret_cast<const int*>(ws + W.ghist),
                              &reinterpret_cast<Control*>(ws + W.control)->status, s));
-        if (y)
+        if (y && !tc)
             PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, false, y + static_cast<size_t>(t0) * d,
                                      ws, W, sms, s));
     }
+    if (tc) return run_stage2_tc(w, L, x, B, all_channels ? nullptr : idx, k, y, ws, W, sms, s);
     return PROX_OK;
 }
 
@@ -226,6 +250,9 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
+    if (use_tc(w, batch, W, sms))
+        return run_stage2_tc(w, L, x, batch, idx, k, y, static_cast<uint8_t*>(ws), W, sms,
+                             static_cast<cudaStream_t>(stream));
     for (int t0 = 0; t0 < batch; t0 += W.TB) {
         const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
         PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb,
@@ -283,6 +310,9 @@ int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, vo
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
+    if (use_tc(w, batch, W, sms))
+        return run_stage2_tc(w, L, x, batch, nullptr, w->d_ff, y, static_cast<uint8_t*>(ws), W,
+                             sms, static_cast<cudaStream_t>(stream));
     for (int t0 = 0; t0 < batch; t0 += W.TB) {
         const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
         PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb, nullptr, w->d_ff, true,

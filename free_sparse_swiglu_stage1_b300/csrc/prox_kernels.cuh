@@ -67,11 +67,23 @@ inline int stage2_blocks(int F, int sms) {
     return sms > need ? sms : need;
 }
 
+// Batch Stage 2 on the tensor cores: batches of more than kTcMinBatch - 1 tokens (padded to
+// BP = 16 MMA columns per bf16 half) run one tcgen05 kernel over the union of all their masks;
+// a block owns at most kTcListMax channels of the union.
+constexpr int kTcMinBatch = 9;
+constexpr int kTcMaxTokens = 16;
+constexpr int kTcListMax = 384;
+inline int tc_tokens(int B) { return B >= kTcMinBatch ? 16 : 0; }
+inline int tc_blocks(int F, int sms) {
+    const int need = (F + kTcListMax - 1) / kTcListMax;
+    return sms > need ? sms : need;
+}
+
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, sigma, idx, ulist, ubits, ypart,
-        total;
-    int TB, P;
+    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, sigma, idx, ulist, ubits, xhl,
+        ypart, total;
+    int TB, P, BPtc;
 };
 
 // Workspace of one call shape. Stage-1 inputs are kept per group of 128 inputs: grows [G][128]
@@ -83,6 +95,7 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     const int G = d / 128;
     W.TB = tile_tokens(d);
     W.P = stage2_blocks(F, sms);
+    W.BPtc = tc_tokens(B);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     W.control = take(sizeof(Control));
@@ -98,7 +111,11 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     W.idx = take(static_cast<size_t>(B) * F * 4);
     W.ulist = take(static_cast<size_t>(F) * 4);
     W.ubits = take(static_cast<size_t>(F) * 4);
-    W.ypart = take(static_cast<size_t>(W.P) * W.TB * d * 4);
+    W.xhl = take(static_cast<size_t>(2) * W.BPtc * d * 2);
+    size_t part = static_cast<size_t>(W.P) * W.TB;
+    if (W.BPtc > 0 && static_cast<size_t>(tc_blocks(F, sms)) * W.BPtc > part)
+        part = static_cast<size_t>(tc_blocks(F, sms)) * W.BPtc;
+    W.ypart = take(part * d * 4);
     W.total = o;
     return W;
 }
@@ -168,6 +185,20 @@ int launch_stage2(const uint8_t* packed, const PackedLayout& L, int d, int F, co
                   int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
                   int count_host, float* y_tile, uint8_t* ws, const WsLayout& W, int sms,
                   cudaStream_t s);
+
+// Sum of per-block partial outputs ypart [P][TB][d] over blocks, in block order, for the
+// first nb rows of each block -> y [nb][d].
+int launch_reduce_partials(const float* ypart, int P, int TB, int d, int nb, float* y,
+                           cudaStream_t s);
+
+// Batch Stage 2 on the tensor cores over a channel list (list == nullptr: every channel,
+// count_host of them) for nb <= kTcMaxTokens tokens; needs a workspace laid out for a batch
+// of at least kTcMinBatch tokens. Splits x into bf16 pairs, runs the MMA kernel, reduces.
+bool stage2_tc_supported(int d, int F, int nb, int sms);
+int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F, const float* x,
+                     int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
+                     int count_host, float* y, uint8_t* ws, const WsLayout& W, int sms,
+                     cudaStream_t s);
 
 // Single-token Stage 2 that selects its channels itself from the salience and Stage 1's
 // histogram (the top-k is folded into the Stage-2 kernel's front end).

@@ -61,7 +61,7 @@ extern "C" int prox_sparse_ffn_noalloc(const prox_packed* w, const float* x, int
         return PROX_ERR_CUDA;
 
     // the scratch this call needs: control block, batch union, per-block partial outputs
-    WsLayout W;
+    WsLayout W{};
     W.TB = tile_tokens(d);
     const int TB = batch < W.TB ? (batch <= 1 ? 1 : (batch <= 2 ? 2 : 4)) : W.TB;
     W.TB = TB;

@@ -558,8 +558,8 @@ static int launch_stage2_t(const uint16_t* rows, int d, int F, const float* x, i
                       sh.NG, kDefaultSpinCycles, status);
 }
 
-static int launch_reduce(const float* ypart, int P, int TB, int d, int nb, float* y_tile,
-                         cudaStream_t s) {
+int launch_reduce_partials(const float* ypart, int P, int TB, int d, int nb, float* y_tile,
+                           cudaStream_t s) {
     const int n4 = d / 4;
     return launch_pdl(reduce_kernel, dim3((n4 + 7) / 8, nb), dim3(256), 0, s,
                       reinterpret_cast<const float4*>(ypart), P, TB, d,
@@ -592,7 +592,7 @@ int launch_stage2(const uint8_t* packed, const PackedLayout& L, int d, int F, co
     PROX_S2(4, 1)
 #undef PROX_S2
     if (rc != PROX_OK) return rc;
-    return launch_reduce(ypart, P, TB, d, nb, y_tile, s);
+    return launch_reduce_partials(ypart, P, TB, d, nb, y_tile, s);
 }
 
 bool stage2_select_supported(int d, int F) {
@@ -625,7 +625,7 @@ int launch_stage2_select(const uint8_t* packed, const PackedLayout& L, int d, in
     PROX_S2S(4)
 #undef PROX_S2S
     if (rc != PROX_OK) return rc;
-    return launch_reduce(ypart, P, 1, d, 1, y, s);
+    return launch_reduce_partials(ypart, P, 1, d, 1, y, s);
 }
 
 }  // namespace prox

@@ -1,0 +1,571 @@
+// Stage 2 of a batch of tokens on the fifth-generation tensor cores (tcgen05, sm_103a).
+//
+// Method: Stage 2 of the Prox FFN ("Prox: two-stage sparse SwiGLU FFN" pages, Stage 2: the
+// selected channels' gate and up rows are multiplied exactly, SiLU(g) * u is formed, and only
+// the matching rows of W_down^T contribute to y). With a batch, the selected set is the union
+// U of the tokens' masks and each token keeps only its own channels:
+//     y_b = sum over j in U with j in M_b of SiLU(x_b . Wg[j]) (x_b . Wu[j]) W_down^T[j].
+// For a batch of up to 16 tokens the two gathered projections are dense contractions over
+// the batch, so they run as tcgen05 MMAs (bf16 operands, fp32 accumulation in tensor memory).
+//
+// Precision: x and h = SiLU(g) u are fp32 on the CUDA-core path. Here each is split into a
+// bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi)), which represents v to about 2^-17 of
+// its size; the pair occupies two columns of the MMA's N dimension (N = 2 * BP for BP padded
+// tokens) and the two halves of the accumulator are added in fp32 afterwards. The weights are
+// bf16 already. Products are exact in fp32 and accumulate in fp32.
+//
+// Work split: one CTA per SM owns a contiguous slice of the union (at most kTcListMax
+// channels). Warps 0..3 copy, warp 4 issues the MMAs, warps 5..8 read the accumulators.
+//   Copies: the gathered rows are brought in by 16-byte cp.async copies from 128 threads (eight
+//     per 128-byte row piece, so each warp copy covers four whole pieces), written straight to
+//     their place in the 128-byte-swizzled canonical layout; each thread's copies complete on
+//     the stage's mbarrier (cp.async.mbarrier.arrive.noinc). A TMA tile::gather4 copy of four
+//     128-byte row pieces was measured to stream at only about 1.9 TB/s on this part, so TMA
+//     carries only the activations here.
+//   Phase A, per M-tile of 128 of the slice's channels: D_gate, D_up [128 x N] accumulate over
+//     d in stages of 64 inputs. The A operand is 128 gathered channel rows x 128 bytes in the
+//     K-major layout; the B operand is the [N x 64] slice of the split activations (one TMA
+//     tile copy).
+//   Epilogue A: a thread owns one channel (one TMEM lane), forms h for every token (zero where
+//     the token did not select the channel) and writes the hi/lo pair into the B operand of
+//     phase B (K-major, no swizzle, resident in shared memory for the whole slice).
+//   Phase B, per tile of 128 outputs: D_y [128 x N] = W_down^T[slice, tile]^T . h, with the
+//     W_down^T rows gathered the same way into the MN-major layout (outputs contiguous),
+//     K = the slice's channels in steps of 16.
+//   Epilogue B: y_b = D_y[:, b] + D_y[:, BP + b] is stored as the block's partial output
+//     ypart[block][b][tile]; a fixed-order reduction over blocks follows (bit-reproducible).
+// Every wait is bounded; a wait that runs out records PROX_ERR_TIMEOUT and the roles leave
+// their loops; copies still in flight are drained (bounded) and tensor memory is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "prox_kernels.cuh"
+
+namespace prox {
+
+namespace {
+
+constexpr int kTcProducers = 128;           // warps 0..3 copy
+constexpr int kTcMmaWarp = 4;               // warp 4 issues the MMAs, warps 5..8 epilogue
+constexpr int kTcThreads = 288;
+constexpr int kTcSlots = 5;                 // ring of stage buffers
+constexpr uint32_t kTcSlotBytes = 36 * 1024;
+constexpr uint32_t kTcUpOff = 16 * 1024;    // phase-A slot: gate rows | up rows | activations
+constexpr uint32_t kTcXOff = 32 * 1024;
+constexpr uint32_t kTcTmemCols = 256;       // A accumulators 2 x 64 columns, D_y 2 x 32
+constexpr uint32_t kTcHSbo = kTcListMax * 16;   // h operand: bytes between 8-row groups
+
+// ------------------------------------------------------------------ tcgen05 / TMA wrappers
+// 16-byte asynchronous copy global -> shared (L2 only, 256-byte L2 fetch granularity).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src)
+                 : "memory");
+}
+// The mbarrier counts one arrival once all of this thread's earlier cp.async copies are done.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tm), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: start address, leading and stride byte offsets (16-byte
+// units), descriptor version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+           (static_cast<uint64_t>(layout) << 61);
+}
+constexpr uint32_t kLayoutNone = 0, kLayoutSw128 = 2;
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness
+// (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Orders this thread's ordinary shared-memory stores before later tensor-core reads.
+__device__ __forceinline__ void fence_smem_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+// ------------------------------------------------------------------ the kernel
+struct TcSmem {
+    uint32_t slots, hop, ch, bits, bars, misc, total;
+};
+__host__ __device__ inline TcSmem tc_smem_layout(int BP) {
+    TcSmem L;
+    uint32_t o = 0;
+    L.slots = o;
+    o += kTcSlots * kTcSlotBytes;
+    L.hop = o;
+    o += static_cast<uint32_t>(2 * BP / 8) * kTcHSbo;
+    L.ch = o;
+    o += kTcListMax * 4;
+    L.bits = o;
+    o += kTcListMax * 4;
+    L.bars = o;
+    o += (2 * kTcSlots + 9) * 8;
+    L.misc = o;
+    o += 64;
+    L.total = o + 1024;   // room to align the base to 1024 bytes
+    return L;
+}
+
+// Barrier indices inside the barrier array.
+constexpr int kBarFull = 0, kBarEmpty = kTcSlots, kBarAFull = 2 * kTcSlots,
+              kBarAEmpty = kBarAFull + 2, kBarBFull = kBarAEmpty + 2, kBarBEmpty = kBarBFull + 2,
+              kBarH = kBarBEmpty + 2, kBarDone = kBarH + 1;
+
+template <int BP>
+__global__ void __launch_bounds__(kTcThreads, 1)
+stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CUtensorMap tm_x,
+                 int d, int F, int nb, const int32_t* __restrict__ list,
+                 const uint32_t* __restrict__ lbits, const int* __restrict__ count_dev,
+                 int count_host, float* __restrict__ ypart, long long spin, int* status) {
+    constexpr int N = 2 * BP;
+    constexpr uint32_t kIdescA = mma_idesc(128, N, 0, 0);
+    constexpr uint32_t kIdescB = mma_idesc(128, N, 1, 0);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const TcSmem SL = tc_smem_layout(BP);
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* sbase = smem_raw + (base - raw);
+    int32_t* s_ch = reinterpret_cast<int32_t*>(sbase + SL.ch);
+    uint32_t* s_bits = reinterpret_cast<uint32_t*>(sbase + SL.bits);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + SL.bars);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + SL.misc);   // [0] tmem, [1] issued, [2] consumed
+    const uint32_t slot0 = base + SL.slots, hop = base + SL.hop;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int i = 0; i < kTcSlots; ++i) {
+            mbar_init(&bars[kBarFull + i], kTcProducers + 1);
+            mbar_init(&bars[kBarEmpty + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[kBarAFull + i], 1);
+            mbar_init(&bars[kBarAEmpty + i], 4);
+            mbar_init(&bars[kBarBFull + i], 1);
+            mbar_init(&bars[kBarBEmpty + i], 4);
+        }
+        mbar_init(&bars[kBarH], 4);
+        mbar_init(&bars[kBarDone], 1);
+        mbar_init_fence();
+        misc[1] = 0;
+        misc[2] = 0;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(&misc[0])),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+
+    grid_dep_wait();
+    grid_dep_launch();
+
+    // this block's slice of the union
+    const int cnt = list ? *count_dev : count_host;
+    const int P = gridDim.x;
+    const int u0 = static_cast<int>(static_cast<long long>(cnt) * blockIdx.x / P);
+    int cb = static_cast<int>(static_cast<long long>(cnt) * (blockIdx.x + 1) / P) - u0;
+    if (cb > kTcListMax || cnt > F) {
+        if (tid == 0) set_status(status, PROX_ERR_BOUNDS);
+        cb = 0;
+    }
+    const int cb16 = (cb + 15) & ~15;
+    const uint32_t all_bits = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
+    for (int i = tid; i < cb16; i += kTcThreads) {
+        int ch = 0;
+        uint32_t bt = 0;
+        if (i < cb) {
+            ch = list ? list[u0 + i] : u0 + i;
+            bt = list ? lbits[u0 + i] : all_bits;
+            if (ch < 0 || ch >= F) {
+                set_status(status, PROX_ERR_BOUNDS);
+                ch = 0;
+                bt = 0;
+            }
+        }
+        s_ch[i] = ch;
+        s_bits[i] = bt;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // padding rows repeat the last channel (finite data; their h is zero)
+    if (cb > 0)
+        for (int i = cb + tid; i < cb16; i += kTcThreads) s_ch[i] = s_ch[cb - 1];
+    __syncthreads();
+    const uint32_t tmem = misc[0];
+
+    const int nmt = (cb + 127) >> 7;       // M-tiles of phase A, K-chunks of phase B
+    const int nka = d >> 6;                // phase-A stages per M-tile
+    const int ntile = d >> 7;              // phase-B output tiles
+
+    if (cb > 0 && tid < kTcProducers) {
+        // ---------------------------------------------------------------- copies
+        // thread p copies 16-byte chunk (p % 8) of row pieces p / 8, p / 8 + 16, ...
+        const size_t pitch = static_cast<size_t>(3) * d;   // elements per packed channel run
+        const int chunk = tid & 7;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int mt = 0; ok && mt < nmt; ++mt) {
+            const int rows = min(128, cb - mt * 128);
+            for (int kc = 0; kc < nka; ++kc, ++it) {
+                const int slot = it % kTcSlots;
+                if (it >= kTcSlots &&
+                    !mbar_wait(&bars[kBarEmpty + slot], ((it / kTcSlots) - 1) & 1, spin, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = slot0 + slot * kTcSlotBytes;
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(&bars[kBarFull + slot], N * 128u);
+                    tma_tile_2d(sb + kTcXOff, &tm_x, kc * 64, 0, &bars[kBarFull + slot]);
+                }
+                // gate pieces (proj 0) then up pieces (proj 1) of the M-tile's rows
+                for (int i = tid >> 3; i < 2 * rows; i += kTcProducers / 8) {
+                    const int proj = i >= rows, r = i - proj * rows;
+                    const uint16_t* src = rows_g + s_ch[mt * 128 + r] * pitch + proj * d +
+                                          kc * 64 + chunk * 8;
+                    const uint32_t dst = sb + proj * kTcUpOff + (r >> 3) * 1024 + (r & 7) * 128 +
+                                         ((chunk ^ (r & 7)) << 4);
+                    cp_async16(dst, src);
+                }
+                cp_async_arrive(&bars[kBarFull + slot]);
+            }
+        }
+        for (int t = 0; ok && t < ntile; ++t) {
+            for (int kc = 0; kc < nmt; ++kc, ++it) {
+                const int rows = min(128, cb - kc * 128);
+                const int r16 = (rows + 15) & ~15;
+                const int slot = it % kTcSlots;
+                if (it >= kTcSlots &&
+                    !mbar_wait(&bars[kBarEmpty + slot], ((it / kTcSlots) - 1) & 1, spin, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = slot0 + slot * kTcSlotBytes;
+                if (tid == 0) mbar_arrive_expect_tx(&bars[kBarFull + slot], 0u);
+                // W_down^T row pieces of 64 outputs: MN-major atoms (8 channels x 128 bytes),
+                // atom (channel group, output half) at group * 2048 + half * 1024
+                for (int i = tid >> 3; i < 2 * r16; i += kTcProducers / 8) {
+                    const int half = i & 1, r = i >> 1;
+                    const uint16_t* src = rows_g + s_ch[kc * 128 + r] * pitch + 2 * d + t * 128 +
+                                          half * 64 + chunk * 8;
+                    const uint32_t dst = sb + (r >> 3) * 2048 + half * 1024 + (r & 7) * 128 +
+                                         ((chunk ^ (r & 7)) << 4);
+                    cp_async16(dst, src);
+                }
+                cp_async_arrive(&bars[kBarFull + slot]);
+            }
+        }
+        cp_async_wait_all();
+        if (tid == 0) misc[1] = it;
+    } else if (cb > 0 && warp == kTcMmaWarp && lane == 0) {
+        // ---------------------------------------------------------------- MMA issue
+        uint32_t it = 0;
+        bool ok = true;
+        for (int mt = 0; ok && mt < nmt; ++mt) {
+            const int buf = mt & 1;
+            if (mt >= 2 && !mbar_wait(&bars[kBarAEmpty + buf], ((mt >> 1) - 1) & 1, spin, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dg = tmem + buf * 64, du = dg + 32;
+            for (int kc = 0; kc < nka; ++kc, ++it) {
+                const int slot = it % kTcSlots;
+                if (!mbar_wait(&bars[kBarFull + slot], (it / kTcSlots) & 1, spin, status)) {
+                    ok = false;
+                    break;
+                }
+                fence_smem_async();   // the copies are ordinary shared-memory writes
+                tc_fence_after();
+                const uint32_t sb = slot0 + slot * kTcSlotBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bx = smem_desc(sb + kTcXOff + ks * 32, 16, 1024, kLayoutSw128);
+                    const uint32_t acc = (kc | ks) != 0;
+                    mma_bf16(dg, smem_desc(sb + ks * 32, 16, 1024, kLayoutSw128), bx, kIdescA, acc);
+                    mma_bf16(du, smem_desc(sb + kTcUpOff + ks * 32, 16, 1024, kLayoutSw128), bx,
+                             kIdescA, acc);
+                }
+                mma_commit(&bars[kBarEmpty + slot]);
+            }
+            if (ok) mma_commit(&bars[kBarAFull + buf]);
+        }
+        if (ok && !mbar_wait(&bars[kBarH], 0, spin, status)) ok = false;
+        tc_fence_after();
+        for (int t = 0; ok && t < ntile; ++t) {
+            const int buf = t & 1;
+            if (t >= 2 && !mbar_wait(&bars[kBarBEmpty + buf], ((t >> 1) - 1) & 1, spin, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t dy = tmem + 128 + buf * 32;
+            for (int kc = 0; kc < nmt; ++kc, ++it) {
+                const int rows = min(128, cb - kc * 128);
+                const int r16 = (rows + 15) & ~15;
+                const int slot = it % kTcSlots;
+                if (!mbar_wait(&bars[kBarFull + slot], (it / kTcSlots) & 1, spin, status)) {
+                    ok = false;
+                    break;
+                }
+                fence_smem_async();
+                tc_fence_after();
+                const uint32_t sb = slot0 + slot * kTcSlotBytes;
+                for (int ks = 0; ks < r16 / 16; ++ks) {
+                    const uint64_t a = smem_desc(sb + ks * 4096, 1024, 2048, kLayoutSw128);
+                    const uint64_t b =
+                        smem_desc(hop + (kc * 16 + ks * 2) * 128, 128, kTcHSbo, kLayoutNone);
+                    mma_bf16(dy, a, b, kIdescB, (kc | ks) != 0);
+                }
+                mma_commit(&bars[kBarEmpty + slot]);
+            }
+            if (ok) mma_commit(&bars[kBarBFull + buf]);
+        }
+        misc[2] = it;
+        // every MMA this thread issued has finished before tensor memory is freed
+        mma_commit(&bars[kBarDone]);
+        mbar_wait(&bars[kBarDone], 0, spin, status);
+    } else if (cb > 0 && warp > kTcMmaWarp) {
+        // ---------------------------------------------------------------- epilogue
+        const int q = warp & 3;               // TMEM lane quarter this warp may read
+        const int m = q * 32 + lane;          // accumulator row of this thread
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        bool ok = true;
+        for (int mt = 0; ok && mt < nmt; ++mt) {
+            const int buf = mt & 1;
+            if (!mbar_wait(&bars[kBarAFull + buf], (mt >> 1) & 1, spin, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float g[N], u[N];
+#pragma unroll
+            for (int c = 0; c < N; c += 16) {
+                tmem_ld16(tmem + lane_off + buf * 64 + c, g + c);
+                tmem_ld16(tmem + lane_off + buf * 64 + 32 + c, u + c);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarAEmpty + buf]);
+            const int cl = mt * 128 + m;
+            if (cl < cb16) {
+                const uint32_t bt = cl < cb ? s_bits[cl] : 0u;
+                unsigned char* hp = sbase + SL.hop + (cl >> 3) * 128 + (cl & 7) * 2;
+#pragma unroll
+                for (int b = 0; b < BP; ++b) {
+                    const float gg = g[b] + g[BP + b];
+                    const float uu = u[b] + u[BP + b];
+                    const float h = ((bt >> b) & 1u) ? silu_f(gg) * uu : 0.f;
+                    const float hi = __bfloat162float(__float2bfloat16_rn(h));
+                    const int nh = b, nl = BP + b;
+                    *reinterpret_cast<uint16_t*>(hp + (nh & 7) * 16 + (nh >> 3) * kTcHSbo) =
+                        bf16_bits(hi);
+                    *reinterpret_cast<uint16_t*>(hp + (nl & 7) * 16 + (nl >> 3) * kTcHSbo) =
+                        bf16_bits(h - hi);
+                }
+            }
+        }
+        fence_smem_async();
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&bars[kBarH]);
+        for (int t = 0; ok && t < ntile; ++t) {
+            const int buf = t & 1;
+            if (!mbar_wait(&bars[kBarBFull + buf], (t >> 1) & 1, spin, status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float v[N];
+#pragma unroll
+            for (int c = 0; c < N; c += 16) tmem_ld16(tmem + lane_off + 128 + buf * 32 + c, v + c);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kBarBEmpty + buf]);
+            float* yp = ypart + static_cast<size_t>(blockIdx.x) * BP * d + t * 128 + m;
+#pragma unroll
+            for (int b = 0; b < BP; ++b)
+                if (b < nb) yp[static_cast<size_t>(b) * d] = v[b] + v[BP + b];
+        }
+    }
+    if (cb == 0) {
+        // an empty slice contributes zeros
+        for (int i = tid; i < nb * d; i += kTcThreads)
+            ypart[static_cast<size_t>(blockIdx.x) * BP * d + i] = 0.f;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        // copies that no MMA consumed (only after a timeout) must land before the block ends
+        const uint32_t issued = misc[1], consumed = misc[2];
+        for (uint32_t it = consumed; it < issued; ++it)
+            mbar_wait(&bars[kBarFull + it % kTcSlots], (it / kTcSlots) & 1, spin, status);
+    }
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTcTmemCols)
+                     : "memory");
+    }
+}
+
+// x [nb][d] fp32 -> xhl [2 BP][d] bf16: rows 0..BP-1 hold bf16(x), rows BP..2BP-1 the
+// remainder bf16(x - bf16(x)); rows of tokens nb..BP-1 are zero.
+__global__ void __launch_bounds__(256)
+split_x_kernel(const float* __restrict__ x, int nb, int d, int BP, uint16_t* __restrict__ xhl) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int total = BP * d;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const float v = i < nb * d ? x[i] : 0.f;
+        const float hi = __bfloat162float(__float2bfloat16_rn(v));
+        xhl[i] = bf16_bits(hi);
+        xhl[total + i] = bf16_bits(v - hi);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map with the 128-byte swizzle: rows x cols elements, row pitch in bytes,
+// box of box_rows x 64 elements.
+int encode_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
+               uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cuda_fail(cudaErrorNotSupported, "looking up cuTensorMapEncodeTiled");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {pitch};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PROX_OK : cuda_fail(cudaErrorInvalidValue, "encoding a tensor map");
+}
+
+template <int BP>
+int launch_tc_t(const uint16_t* rows, const CUtensorMap& tm_x, int d, int F, int nb,
+                const int32_t* list, const uint32_t* lbits, const int* count_dev, int count_host,
+                float* ypart, int P, int* status, cudaStream_t s) {
+    const size_t smem = tc_smem_layout(BP).total;
+    auto fn = stage2_tc_kernel<BP>;
+    if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
+    return launch_pdl(fn, dim3(P), dim3(kTcThreads), smem, s, rows, tm_x, d, F, nb, list, lbits,
+                      count_dev, count_host, ypart, kDefaultSpinCycles, status);
+}
+
+}  // namespace
+
+bool stage2_tc_supported(int d, int F, int nb, int sms) {
+    return nb >= 1 && nb <= kTcMaxTokens && d % 128 == 0 &&
+           static_cast<long long>(tc_blocks(F, sms)) * kTcListMax >= F;
+}
+
+int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F, const float* x,
+                     int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
+                     int count_host, float* y, uint8_t* ws, const WsLayout& W, int sms,
+                     cudaStream_t s) {
+    if (!stage2_tc_supported(d, F, nb, sms) || W.BPtc < nb) return PROX_ERR_UNSUPPORTED;
+    const int BP = W.BPtc;
+    const int P = tc_blocks(F, sms);
+    uint16_t* xhl = reinterpret_cast<uint16_t*>(ws + W.xhl);
+    float* ypart = reinterpret_cast<float*>(ws + W.ypart);
+    int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
+    const uint16_t* rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
+    CUtensorMap tm_x;
+    if (encode_map(&tm_x, xhl, d, 2 * BP, static_cast<uint64_t>(2) * d, 2 * BP) != PROX_OK)
+        return PROX_ERR_CUDA;
+    const int total = BP * d;
+    int rc = launch_pdl(split_x_kernel, dim3((total + 1023) / 1024), dim3(256), 0, s, x, nb, d, BP,
+                        xhl);
+    if (rc != PROX_OK) return rc;
+    rc = BP == 16 ? launch_tc_t<16>(rows, tm_x, d, F, nb, list, lbits, count_dev, count_host,
+                                    ypart, P, status, s)
+                  : PROX_ERR_UNSUPPORTED;
+    if (rc != PROX_OK) return rc;
+    return launch_reduce_partials(ypart, P, BP, d, nb, y, s);
+}
+
+}  // namespace prox
