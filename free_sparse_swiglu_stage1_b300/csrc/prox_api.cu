@@ -88,21 +88,23 @@ int run_stage2_tile(const prox_packed* w, const PackedLayout& L, const float* xt
                          sms, s);
 }
 
-// Stage 2 of a whole batch on the tensor cores: one pass over the union of every token's mask
-// (idx == nullptr: every channel).
+// Stage 2 of a whole batch on the tensor cores: one pass over the union of every token's mask.
+// bits: the batch's channel bitmap (nullptr: every channel); if idx is given instead, the
+// bitmap is built from it first.
 int run_stage2_tc(const prox_packed* w, const PackedLayout& L, const float* x, int B,
-                  const int32_t* idx, int k, float* y, uint8_t* ws, const WsLayout& W, int sms,
-                  cudaStream_t s) {
+                  const int32_t* idx, int k, const uint32_t* bits, float* y, uint8_t* ws,
+                  const WsLayout& W, int sms, cudaStream_t s) {
     const int d = w->d_model, F = w->d_ff;
     const uint8_t* packed = static_cast<const uint8_t*>(w->base);
-    if (!idx)
-        return launch_stage2_tc(packed, L, d, F, x, B, nullptr, nullptr, nullptr, F, y, ws, W, sms, s);
-    Control* ctrl = reinterpret_cast<Control*>(ws + W.control);
-    int32_t* ulist = reinterpret_cast<int32_t*>(ws + W.ulist);
-    uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
-    PROX_TRY(launch_union(idx, B, k, F, ulist, ubits, &ctrl->union_count, &ctrl->status, s));
-    return launch_stage2_tc(packed, L, d, F, x, B, ulist, ubits, &ctrl->union_count, 0, y, ws, W,
-                            sms, s);
+    if (idx) {
+        uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
+        Control* ctrl = reinterpret_cast<Control*>(ws + W.control);
+        PROX_TRY(cuda_ok(cudaMemsetAsync(ubits, 0, static_cast<size_t>(F) * 4, s),
+                         "clearing the channel bitmap"));
+        PROX_TRY(launch_mask_bits(idx, B, k, F, ubits, &ctrl->status, s));
+        bits = ubits;
+    }
+    return launch_stage2_tc(packed, L, d, F, x, B, bits, y, ws, W, sms, s);
 }
 
 bool use_tc(const prox_packed* w, int B, const WsLayout& W, int sms) {
@@ -120,11 +122,13 @@ struct Debug {
 // Test hook of the single-token path whose Stage 2 selects its channels itself.
 int32_t* g_fused_sel = nullptr;
 
-// The whole path over all tiles. y == nullptr stops after the mask.
+// The whole path. y == nullptr stops after the mask. Stage 1 and the top-k run once for
+// all B tokens (in tiles of W.TB tokens inside each kernel); Stage 2 runs per tile on the
+// CUDA cores, or once for the batch on the tensor cores.
 int run_path(const prox_packed* w, const float* x, int B, double sparsity, double in_sparsity,
              float* y, int32_t* idx_out, uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s,
              const Debug* dbg) {
-    const int d = w->d_model, F = w->d_ff, G = d / 128;
+    const int d = w->d_model, F = w->d_ff;
     const PackedLayout L = packed_layout(d, F);
     const uint8_t* packed = static_cast<const uint8_t*>(w->base);
     const int k = k_rule(sparsity, F);
@@ -132,44 +136,41 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
     const bool all_channels = (k == F) && !dbg;
     int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + W.idx);
     float* sigma = (dbg && dbg->salience) ? dbg->salience : reinterpret_cast<float*>(ws + W.sigma);
-    // a large batch makes every tile's mask first, then one tensor-core Stage 2 over them all
+    int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
+    uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
     const bool tc = y && !dbg && use_tc(w, B, W, sms);
+    if (all_channels) {
+        // sparsity 0: every channel is kept, the ranking cannot change the result
+        if (idx_out) PROX_TRY(launch_iota(idx, F, B, s));
+        if (!y) return PROX_OK;
+        if (tc) return run_stage2_tc(w, L, x, B, nullptr, F, nullptr, y, ws, W, sms, s);
+        for (int t0 = 0; t0 < B; t0 += W.TB) {
+            const int nb = B - t0 < W.TB ? B - t0 : W.TB;
+            PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb, nullptr, F, true,
+                                     y + static_cast<size_t>(t0) * d, ws, W, sms, s));
+        }
+        return PROX_OK;
+    }
+    PROX_TRY(launch_input_quant(x, d, F, B, k_in, ws, W, tc ? ubits : nullptr,
+                                dbg ? dbg->qx : nullptr, dbg ? dbg->sx : nullptr, s));
+    PROX_TRY(launch_stage1(packed, L, d, F, B, ws, W, sigma, dbg ? dbg->acc_gate : nullptr,
+                           dbg ? dbg->acc_up : nullptr, sms, s));
+    if (dbg) return PROX_OK;
+    const int* ghist = reinterpret_cast<const int*>(ws + W.ghist);
+    if (g_fused_sel && y && !idx_out && B == 1 && stage2_select_supported(d, F)) {
+        // one token, mask not wanted: Stage 2 selects its channels itself
+        return launch_stage2_select(packed, L, d, F, x, sigma, ghist, k, y, g_fused_sel, ws, W,
+                                    sms, s);
+    }
+    PROX_TRY(launch_topk(sigma, F, B, k, idx, ghist, tc ? ubits : nullptr, status, s));
+    if (!y) return PROX_OK;
+    if (tc) return run_stage2_tc(w, L, x, B, nullptr, k, ubits, y, ws, W, sms, s);
     for (int t0 = 0; t0 < B; t0 += W.TB) {
         const int nb = B - t0 < W.TB ? B - t0 : W.TB;
-        const float* xt = x + static_cast<size_t>(t0) * d;
-        int32_t* idx_t = idx + static_cast<size_t>(t0) * k;
-        if (all_channels) {
-            // sparsity 0: every channel is kept, the ranking cannot change the result
-            if (idx_out) PROX_TRY(launch_iota(idx_t, F, nb, s));
-            if (y && !tc)
-                PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, true,
-                                         y + static_cast<size_t>(t0) * d, ws, W, sms, s));
-            continue;
-        }
-        PROX_TRY(launch_input_quant(xt, d, nb, k_in, ws, W,
-                                    dbg && dbg->qx ? dbg->qx + static_cast<size_t>(t0) * d : nullptr,
-                                    dbg && dbg->sx ? dbg->sx + static_cast<size_t>(t0) * G : nullptr, s));
-        PROX_TRY(launch_stage1(packed, L, d, F, nb, k_in, ws, W, sigma + static_cast<size_t>(t0) * F,
-                               dbg && dbg->acc_gate ? dbg->acc_gate + static_cast<size_t>(t0) * G * F : nullptr,
-                               dbg && dbg->acc_up ? dbg->acc_up + static_cast<size_t>(t0) * G * F : nullptr,
-                               sms, s));
-        if (dbg) continue;
-        if (g_fused_sel && y && !idx_out && nb == 1 && stage2_select_supported(d, F)) {
-            // one token, mask not wanted: Stage 2 selects its channels itself
-            PROX_TRY(launch_stage2_select(packed, L, d, F, xt, sigma + static_cast<size_t>(t0) * F,
-                                          reinterpret_cast<const int*>(ws + W.ghist), k,
-                                          y + static_cast<size_t>(t0) * d, g_fused_sel, ws, W, sms,
-                                          s));
-            continue;
-        }
-        PROX_TRY(launch_topk(sigma + static_cast<size_t>(t0) * F, F, nb, k, idx_t,
-                             reinterpret_cast<const int*>(ws + W.ghist),
-                             &reinterpret_cast<Control*>(ws + W.control)->status, s));
-        if (y && !tc)
-            PROX_TRY(run_stage2_tile(w, L, xt, nb, idx_t, k, false, y + static_cast<size_t>(t0) * d,
-                                     ws, W, sms, s));
+        PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb,
+                                 idx + static_cast<size_t>(t0) * k, k, false,
+                                 y + static_cast<size_t>(t0) * d, ws, W, sms, s));
     }
-    if (tc) return run_stage2_tc(w, L, x, B, all_channels ? nullptr : idx, k, y, ws, W, sms, s);
     return PROX_OK;
 }
 
@@ -251,8 +252,8 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
     if (use_tc(w, batch, W, sms))
-        return run_stage2_tc(w, L, x, batch, idx, k, y, static_cast<uint8_t*>(ws), W, sms,
-                             static_cast<cudaStream_t>(stream));
+        return run_stage2_tc(w, L, x, batch, idx, k, nullptr, y, static_cast<uint8_t*>(ws), W,
+                             sms, static_cast<cudaStream_t>(stream));
     for (int t0 = 0; t0 < batch; t0 += W.TB) {
         const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
         PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb,
@@ -311,8 +312,8 @@ int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, vo
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
     if (use_tc(w, batch, W, sms))
-        return run_stage2_tc(w, L, x, batch, nullptr, w->d_ff, y, static_cast<uint8_t*>(ws), W,
-                             sms, static_cast<cudaStream_t>(stream));
+        return run_stage2_tc(w, L, x, batch, nullptr, w->d_ff, nullptr, y,
+                             static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream));
     for (int t0 = 0; t0 < batch; t0 += W.TB) {
         const int nb = batch - t0 < W.TB ? batch - t0 : W.TB;
         PROX_TRY(run_stage2_tile(w, L, x + static_cast<size_t>(t0) * d, nb, nullptr, w->d_ff, true,

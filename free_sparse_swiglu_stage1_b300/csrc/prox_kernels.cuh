@@ -27,6 +27,13 @@ inline PackedLayout packed_layout(int d, int F) {
 // Tokens are processed in tiles whose Stage-2 activations and partial outputs live in
 // registers; wider rows leave room for fewer tokens per tile.
 inline int tile_tokens(int d) { return d <= 4096 ? 4 : (d <= 8192 ? 2 : 1); }
+// Token width of the Stage-1 kernel for B tokens in tiles of TB: the whole batch if it fits
+// one tile (1, 2 or 4), else the tile width.
+inline int stage1_width(int B, int TB) {
+    const int n = B < TB ? B : TB;
+    return n <= 1 ? 1 : (n <= 2 ? 2 : 4);
+}
+inline int token_tiles(int B, int TB) { return (B + TB - 1) / TB; }
 
 // Stage 1 work split. A warp reads one kept input row's codes for 32 * CPL channels with
 // one load of CPL bytes per lane (CPL = 16 for one token, 8 for two, 4 for four: the
@@ -67,13 +74,14 @@ inline int stage2_blocks(int F, int sms) {
     return sms > need ? sms : need;
 }
 
-// Batch Stage 2 on the tensor cores: batches of more than kTcMinBatch - 1 tokens (padded to
-// BP = 16 MMA columns per bf16 half) run one tcgen05 kernel over the union of all their masks;
-// a block owns at most kTcListMax channels of the union.
-constexpr int kTcMinBatch = 9;
+// Batch Stage 2 on the tensor cores: a batch of kTcMinBatch or more tokens (padded to BP = 8
+// or 16 MMA columns per bf16 half) runs one tcgen05 kernel over the union of all their
+// masks; a block owns at most kTcListMax channels of the union. A single token stays on the
+// CUDA cores (a GEMV; its bulk-copy stream is the faster one).
+constexpr int kTcMinBatch = 2;
 constexpr int kTcMaxTokens = 16;
 constexpr int kTcListMax = 384;
-inline int tc_tokens(int B) { return B >= kTcMinBatch ? 16 : 0; }
+inline int tc_tokens(int B) { return B < kTcMinBatch ? 0 : (B <= 8 ? 8 : 16); }
 inline int tc_blocks(int F, int sms) {
     const int need = (F + kTcListMax - 1) / kTcListMax;
     return sms > need ? sms : need;
@@ -86,10 +94,12 @@ struct WsLayout {
     int TB, P, BPtc;
 };
 
-// Workspace of one call shape. Stage-1 inputs are kept per group of 128 inputs: grows [G][128]
-// (the group's kept inputs, ascending, padded to a multiple of 4 with copies of the last),
-// gcnt [G] (padded counts), gq [G + 1] (quad offsets: exclusive sums of gcnt / 4),
-// gqx [TB][G][128] int8 codes, sx [TB][G] scales.
+// Workspace of one call shape. Stage-1 inputs are kept per token tile and per group of 128
+// inputs: grows [G][128] (the group's kept inputs, ascending, padded to a multiple of 4 with
+// copies of the last), gcnt [G] (padded counts), gq [G + 1] (quad offsets: exclusive sums of
+// gcnt / 4), gqx [TB][G][128] int8 codes, sx [TB][G] scales, ghist [TB][2048]; each of these
+// is repeated for every tile of TB tokens. ubits [F] holds the batch union's token bits
+// (compacted with ulist on the CUDA-core path, one word per channel on the tensor-core path).
 inline WsLayout ws_layout(int d, int F, int B, int sms) {
     WsLayout W;
     const int G = d / 128;
@@ -101,12 +111,13 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     W.control = take(sizeof(Control));
     W.xbuf = take(static_cast<size_t>(B) * d * 4);
     W.ybuf = take(static_cast<size_t>(B) * d * 4);
-    W.grows = take(static_cast<size_t>(d) * 4);
-    W.gqx = take(static_cast<size_t>(W.TB) * d);
-    W.gcnt = take(static_cast<size_t>(G) * 4);
-    W.gq = take(static_cast<size_t>(G + 1) * 4);
-    W.sx = take(static_cast<size_t>(W.TB) * G * 4);
-    W.ghist = take(static_cast<size_t>(W.TB) * 2048 * 4);
+    const size_t nt = static_cast<size_t>(token_tiles(B, W.TB));   // per-tile buffers below
+    W.grows = take(nt * d * 4);
+    W.gqx = take(nt * W.TB * d);
+    W.gcnt = take(nt * G * 4);
+    W.gq = take(nt * (G + 1) * 4);
+    W.sx = take(nt * W.TB * G * 4);
+    W.ghist = take(nt * W.TB * 2048 * 4);
     W.sigma = take(static_cast<size_t>(B) * F * 4);
     W.idx = take(static_cast<size_t>(B) * F * 4);
     W.ulist = take(static_cast<size_t>(F) * 4);
@@ -161,20 +172,30 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 int launch_pack(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down, int d,
                 int F, const PackedLayout& L, uint8_t* base, cudaStream_t s);
 
-// Input selection + activation quantization for one tile of nb tokens (Stage 1 inputs).
-// Also clears the tile's salience histograms (ws + W.ghist) that Stage 1 fills for the top-k.
-int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, const WsLayout& W,
-                       int8_t* dbg_qx, float* dbg_sx, cudaStream_t s);
+// Input selection + activation quantization (Stage 1 inputs) for all B tokens, one block
+// per tile of W.TB tokens. Also clears the tiles' salience histograms (ws + W.ghist) that
+// Stage 1 fills for the top-k, and zbits [F] (if not null) for the top-k's channel bitmap.
+int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* ws,
+                       const WsLayout& W, uint32_t* zbits, int8_t* dbg_qx, float* dbg_sx,
+                       cudaStream_t s);
 
-// Stage-1 proxy projections + salience for one tile.
-int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb, int k_in,
-                  uint8_t* ws, const WsLayout& W, float* sigma_tile, int32_t* dbg_gate,
-                  int32_t* dbg_up, int sms, cudaStream_t s);
+// Stage-1 proxy projections + salience for all B tokens (grid z: token tiles);
+// sigma [B][F].
+int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int B, uint8_t* ws,
+                  const WsLayout& W, float* sigma, int32_t* dbg_gate, int32_t* dbg_up, int sms,
+                  cudaStream_t s);
 
-// Per-token top-k of the salience -> ascending channel indices (row stride k). ghist, if not
-// null, holds per token the 2048-bin histogram of the salience bits 30..20 (Stage 1 builds it).
-int launch_topk(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
-                const int* ghist, int* status, cudaStream_t s);
+// Per-token top-k of the salience [B][F] -> ascending channel indices (row stride k), one
+// block per token. ghist, if not null, holds per token the 2048-bin histogram of the
+// salience bits 30..20 (Stage 1 builds it). bits, if not null, receives bit b of every
+// channel token b selected (atomic OR; the caller clears it first).
+int launch_topk(const float* sigma, int F, int B, int k, int32_t* idx, const int* ghist,
+                uint32_t* bits, int* status, cudaStream_t s);
+
+// bits [F] |= (1 << b) for every channel of idx row b (rows of length k, B <= 32); the
+// caller clears bits first.
+int launch_mask_bits(const int32_t* idx, int B, int k, int F, uint32_t* bits, int* status,
+                     cudaStream_t s);
 
 // Union of nb index rows (row stride k) -> ascending list + per-entry token bits + count.
 int launch_union(const int32_t* idx_tile, int nb, int k, int F, int32_t* ulist, uint32_t* ubits,
@@ -191,14 +212,14 @@ int launch_stage2(const uint8_t* packed, const PackedLayout& L, int d, int F, co
 int launch_reduce_partials(const float* ypart, int P, int TB, int d, int nb, float* y,
                            cudaStream_t s);
 
-// Batch Stage 2 on the tensor cores over a channel list (list == nullptr: every channel,
-// count_host of them) for nb <= kTcMaxTokens tokens; needs a workspace laid out for a batch
-// of at least kTcMinBatch tokens. Splits x into bf16 pairs, runs the MMA kernel, reduces.
+// Batch Stage 2 on the tensor cores over the channels whose word in bits [F] is nonzero
+// (bit b: token b selected the channel; bits == nullptr: every channel for every token) for
+// nb <= kTcMaxTokens tokens; needs a workspace laid out for a batch of at least kTcMinBatch
+// tokens. Splits x into bf16 pairs, runs the MMA kernel, reduces.
 bool stage2_tc_supported(int d, int F, int nb, int sms);
 int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F, const float* x,
-                     int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
-                     int count_host, float* y, uint8_t* ws, const WsLayout& W, int sms,
-                     cudaStream_t s);
+                     int nb, const uint32_t* bits, float* y, uint8_t* ws, const WsLayout& W,
+                     int sms, cudaStream_t s);
 
 // Single-token Stage 2 that selects its channels itself from the salience and Stage 1's
 // histogram (the top-k is folded into the Stage-2 kernel's front end).

@@ -9,9 +9,12 @@
 //               the candidates of one bin are scanned again. One scan in index order then
 //               emits the mask as ascending channel indices, giving equal values to the
 //               lower index.
-// union_kernel  batch path: the tile's per-token masks are merged into one ascending list
-//               of channels and a bit mask per entry telling which tokens selected it, so
-//               Stage 2 reads each selected row once for the whole tile.
+//               With a channel bitmap given, each block also ORs its token's bit into the
+//               word of every channel it selected (the tensor-core Stage 2 reads it).
+// union_kernel  CUDA-core batch path: the tile's per-token masks are merged into one
+//               ascending list of channels and a bit mask per entry telling which tokens
+//               selected it, so Stage 2 reads each selected row once for the whole tile.
+// mask_bits_kernel  the bitmap of given masks (for the tensor-core Stage 2).
 #include "prox_kernels.cuh"
 
 namespace prox {
@@ -21,7 +24,8 @@ constexpr int kTopkThreads = 1024;
 template <int NT, int RUN>
 __global__ void __launch_bounds__(NT)
 topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__ idx,
-            const int* __restrict__ ghist, long long spin, int* __restrict__ status) {
+            const int* __restrict__ ghist, uint32_t* __restrict__ bits, long long spin,
+            int* __restrict__ status) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);   // [F] salience bits (all >= 0)
     __shared__ __align__(128) int hist[2 * 2048];
@@ -61,6 +65,24 @@ topk_kernel(const float* __restrict__ sigma, int F, int k, int32_t* __restrict__
     __syncthreads();
     int32_t* out = idx + static_cast<size_t>(b) * k;
     for (int i = tid; i < k; i += NT) out[i] = s_idx[i];
+    if (bits)   // the batch's channel bitmap for the tensor-core Stage 2
+        for (int i = tid; i < k; i += NT) atomicOr(&bits[s_idx[i]], 1u << b);
+}
+
+// bits[j] |= 1 << b for every channel j of index row b; grid (chunks of the rows, B).
+__global__ void __launch_bounds__(256)
+mask_bits_kernel(const int32_t* __restrict__ idx, int k, int F, uint32_t* __restrict__ bits,
+                 int* __restrict__ status) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int b = blockIdx.y;
+    for (int i = blockIdx.x * 256 + threadIdx.x; i < k; i += gridDim.x * 256) {
+        const int j = idx[static_cast<size_t>(b) * k + i];
+        if (j >= 0 && j < F)
+            atomicOr(&bits[j], 1u << b);
+        else if (status)
+            set_status(status, PROX_ERR_BOUNDS);
+    }
 }
 
 __global__ void __launch_bounds__(kTopkThreads)
@@ -100,25 +122,32 @@ union_kernel(const int32_t* __restrict__ idx, int nb, int k, int F, int32_t* __r
 }
 
 template <int NT, int RUN>
-static int launch_topk_t(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
-                         const int* ghist, int* status, cudaStream_t s) {
+static int launch_topk_t(const float* sigma, int F, int B, int k, int32_t* idx,
+                         const int* ghist, uint32_t* bits, int* status, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(F) * 4;
     auto fn = topk_kernel<NT, RUN>;
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    return launch_pdl(fn, dim3(nb), dim3(NT), smem, s, sigma_tile, F, k, idx_tile, ghist,
+    return launch_pdl(fn, dim3(B), dim3(NT), smem, s, sigma, F, k, idx, ghist, bits,
                       kDefaultSpinCycles, status);
 }
 
-int launch_topk(const float* sigma_tile, int F, int nb, int k, int32_t* idx_tile,
-                const int* ghist, int* status, cudaStream_t s) {
+int launch_topk(const float* sigma, int F, int B, int k, int32_t* idx, const int* ghist,
+                uint32_t* bits, int* status, cudaStream_t s) {
     switch (select_run(F, 1024)) {
-        case 4: return launch_topk_t<1024, 4>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
-        case 8: return launch_topk_t<1024, 8>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
-        case 16: return launch_topk_t<1024, 16>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
-        case 32: return launch_topk_t<1024, 32>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
-        case 64: return launch_topk_t<1024, 64>(sigma_tile, F, nb, k, idx_tile, ghist, status, s);
+        case 4: return launch_topk_t<1024, 4>(sigma, F, B, k, idx, ghist, bits, status, s);
+        case 8: return launch_topk_t<1024, 8>(sigma, F, B, k, idx, ghist, bits, status, s);
+        case 16: return launch_topk_t<1024, 16>(sigma, F, B, k, idx, ghist, bits, status, s);
+        case 32: return launch_topk_t<1024, 32>(sigma, F, B, k, idx, ghist, bits, status, s);
+        case 64: return launch_topk_t<1024, 64>(sigma, F, B, k, idx, ghist, bits, status, s);
         default: return PROX_ERR_UNSUPPORTED;
     }
+}
+
+int launch_mask_bits(const int32_t* idx, int B, int k, int F, uint32_t* bits, int* status,
+                     cudaStream_t s) {
+    int chunks = (k + 255) / 256;
+    if (chunks > 16) chunks = 16;
+    return launch_pdl(mask_bits_kernel, dim3(chunks, B), dim3(256), 0, s, idx, k, F, bits, status);
 }
 
 int launch_union(const int32_t* idx_tile, int nb, int k, int F, int32_t* ulist, uint32_t* ubits,

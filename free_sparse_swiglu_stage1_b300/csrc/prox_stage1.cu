@@ -10,7 +10,8 @@
 //   last one, whose codes are 0) with every token's int8 codes; no global compaction is
 //   needed, since each group's list has a fixed place.
 //
-// stage1_kernel (grid: channel tiles x slices of consecutive groups, 8 warps per block)
+// stage1_kernel (grid: channel tiles x slices of consecutive groups x token tiles, 8 warps
+// per block)
 //   The "fused split-N" design: a block owns a tile of 32 * CPL channels and the kept rows
 //   of a few groups; a kept input is one contiguous run of CPL bytes per lane (gate | up
 //   nibbles of CPL channels), so rejected inputs cost no bytes and a warp reads a row with
@@ -36,17 +37,19 @@ constexpr int kSelThreads = 1024;
 constexpr int kS1Threads = 256;
 constexpr int kS1Warps = kS1Threads / 32;
 
-// Input selection and activation codes for one tile of nb tokens (see the file comment).
-// Thread t owns the run of inputs [t*RUN, t*RUN + RUN), RUN a power of two in [4, 16], so a
-// run lies inside one group of 128 and a group's runs are 128/RUN aligned lanes of one warp.
-// Outputs: grows [G][128], gcnt [G], gq [G + 1], gqx [TB][G][128], sx [TB][G]; clears
-// ghist [TB][2048].
+// Input selection and activation codes (see the file comment); block z handles token tile z
+// (tokens z*TB .. z*TB + nb - 1 of the B). Thread t owns the run of inputs
+// [t*RUN, t*RUN + RUN), RUN a power of two in [4, 16], so a run lies inside one group of 128
+// and a group's runs are 128/RUN aligned lanes of one warp. Outputs per tile: grows [G][128],
+// gcnt [G], gq [G + 1], gqx [TB][G][128] (TBs rows written: the Stage-1 kernel's token
+// width), sx [TB][G]; clears the tile's ghist [TB][2048] and, in block 0, zbits [F] if given.
 template <int RUN>
 __global__ void __launch_bounds__(kSelThreads)
-input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
+input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, int k_in,
                    int* __restrict__ grows, int* __restrict__ gcnt, int* __restrict__ gq,
                    int8_t* __restrict__ gqx, float* __restrict__ sx_ws, int* __restrict__ ghist,
-                   int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx) {
+                   uint32_t* __restrict__ zbits, int F, int8_t* __restrict__ dbg_qx,
+                   float* __restrict__ dbg_sx) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                 // [d]
     int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);                   // [TB][d]
@@ -61,12 +64,24 @@ input_quant_kernel(const float* __restrict__ x, int d, int nb, int TB, int k_in,
     const int g_mine = lo >> 7;
     const bool active = lo < hi;
     const int gl = tid & (tpg - 1);                // this thread's place among its group's
-    const int TBs = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);   // tokens the Stage-1 kernel reads
+    const int z = blockIdx.x, t0 = z * TB;
+    const int nb = min(TB, B - t0);
+    x += static_cast<size_t>(t0) * d;
+    grows += static_cast<size_t>(z) * d;
+    gcnt += static_cast<size_t>(z) * G;
+    gq += static_cast<size_t>(z) * (G + 1);
+    gqx += static_cast<size_t>(z) * TB * d;
+    sx_ws += static_cast<size_t>(z) * TB * G;
+    ghist += static_cast<size_t>(z) * TB * 2048;
+    if (dbg_qx) dbg_qx += static_cast<size_t>(t0) * d;
+    if (dbg_sx) dbg_sx += static_cast<size_t>(t0) * G;
 
     grid_dep_wait();
     grid_dep_launch();
     for (int i = tid; i < TB * 512; i += NT)   // filled by Stage 1 for the top-k
         reinterpret_cast<int4*>(ghist)[i] = make_int4(0, 0, 0, 0);
+    if (zbits && z == 0)   // the batch's channel bitmap, filled by the top-k
+        for (int i = tid; i < F; i += NT) zbits[i] = 0u;
     uint64_t any = 0ull;
     for (int b = 0; b < nb; ++b) {
         float xv[RUN];
@@ -214,7 +229,7 @@ __global__ void __launch_bounds__(kS1Threads, 2)
 stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ scales, int d, int F,
               const int* __restrict__ grows, const int* __restrict__ gq,
               const int8_t* __restrict__ gqx, const float* __restrict__ sx, int gps, int S,
-              int nb, float* __restrict__ sigma, int* __restrict__ ghist,
+              int B, float* __restrict__ sigma, int* __restrict__ ghist,
               int32_t* __restrict__ dbg_gate, int32_t* __restrict__ dbg_up,
               int* __restrict__ status) {
     constexpr int NV = 2 * CPL * TB;       // values per lane: (token, channel, projection)
@@ -229,9 +244,19 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     int* s_qs = reinterpret_cast<int*>(s_sx + TB * gps);                   // [gps + 1] quad starts
     __shared__ DF s_part[NV * 32];   // this slice's double-float sums, read by the whole cluster
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int tile = blockIdx.x, s = blockIdx.y;
+    const int tile = blockIdx.x, s = blockIdx.y, z = blockIdx.z;
     const int G = d >> 7;
     const int g0 = s * gps, ng = min(gps, G - g0);
+    // token tile z: tokens z*TB .. z*TB + nb - 1
+    const int nb = min(TB, B - z * TB);
+    grows += static_cast<size_t>(z) * d;
+    gq += static_cast<size_t>(z) * (G + 1);
+    gqx += static_cast<size_t>(z) * TB * d;
+    sx += static_cast<size_t>(z) * TB * G;
+    ghist += static_cast<size_t>(z) * TB * 2048;
+    sigma += static_cast<size_t>(z) * TB * F;
+    if (dbg_gate) dbg_gate += static_cast<size_t>(z) * TB * G * F;
+    if (dbg_up) dbg_up += static_cast<size_t>(z) * TB * G * F;
     const int c0 = tile * TILE + lane * CPL;          // this lane's first channel
     const bool valid = c0 < F;                        // F % 16 == 0: all CPL channels or none
     const uint8_t* cbase = codes + (valid ? c0 : 0);
@@ -340,24 +365,57 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
             }
         }
     };
-    uint32_t wa[4][NWC], wb[4][NWC];
-    if (qa < qb) load_quad(wa, qa, gl);
-    for (int q = qa; q < qb; q += 2) {
-        // quad q is in wa; load quad q + 1 into wb, then q + 2 into wa after q is done
-        int g1 = gl;
-        if (q + 1 < qb) {
-            while (g1 + 1 < ng && s_qs[g1 + 1] <= q + 1) ++g1;
-            load_quad(wb, q + 1, g1);
+    if constexpr (CPL == 16) {
+        // 16-byte loads: two quads in flight keep enough bytes in flight
+        uint32_t wa[4][NWC], wb[4][NWC];
+        if (qa < qb) load_quad(wa, qa, gl);
+        for (int q = qa; q < qb; q += 2) {
+            // quad q is in wa; load quad q + 1 into wb, then q + 2 into wa after q is done
+            int g1 = gl;
+            if (q + 1 < qb) {
+                while (g1 + 1 < ng && s_qs[g1 + 1] <= q + 1) ++g1;
+                load_quad(wb, q + 1, g1);
+            }
+            step(wa, q, gl, g1, q + 1 == qb);
+            if (q + 1 >= qb) break;
+            int g2 = g1;
+            if (q + 2 < qb) {
+                while (g2 + 1 < ng && s_qs[g2 + 1] <= q + 2) ++g2;
+                load_quad(wa, q + 2, g2);
+            }
+            step(wb, q + 1, g1, g2, q + 2 == qb);
+            gl = g2;
         }
-        step(wa, q, gl, g1, q + 1 == qb);
-        if (q + 1 >= qb) break;
-        int g2 = g1;
-        if (q + 2 < qb) {
-            while (g2 + 1 < ng && s_qs[g2 + 1] <= q + 2) ++g2;
-            load_quad(wa, q + 2, g2);
+    } else {
+        // narrower loads: a ring of kQ quads in flight; slot j holds quads j, j + kQ, ...
+        constexpr int kQ = 4;
+        uint32_t wr[kQ][4][NWC];
+        int gs[kQ];   // group of the quad in each slot
+        int gt = gl;  // group of the last quad loaded
+#pragma unroll
+        for (int j = 0; j < kQ; ++j) {
+            gs[j] = gt;
+            if (qa + j < qb) {
+                while (gt + 1 < ng && s_qs[gt + 1] <= qa + j) ++gt;
+                gs[j] = gt;
+                load_quad(wr[j], qa + j, gt);
+            }
         }
-        step(wb, q + 1, g1, g2, q + 2 == qb);
-        gl = g2;
+        for (int q0 = qa; q0 < qb; q0 += kQ) {
+#pragma unroll
+            for (int j = 0; j < kQ; ++j) {
+                const int q = q0 + j;
+                if (q >= qb) break;
+                // slot j + 1 (mod kQ) holds quad q + 1 when there is one
+                step(wr[j], q, gs[j], q + 1 < qb ? gs[(j + 1) % kQ] : gs[j], q + 1 == qb);
+                const int qn = q + kQ;
+                if (qn < qb) {
+                    while (gt + 1 < ng && s_qs[gt + 1] <= qn) ++gt;
+                    gs[j] = gt;
+                    load_quad(wr[j], qn, gt);
+                }
+            }
+        }
     }
     __syncthreads();
 
@@ -420,23 +478,25 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
     cluster.sync();   // no block leaves while another still reads its shared memory
 }
 
-int launch_input_quant(const float* x, int d, int nb, int k_in, uint8_t* ws, const WsLayout& W,
-                       int8_t* dbg_qx, float* dbg_sx, cudaStream_t s) {
+int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* ws,
+                       const WsLayout& W, uint32_t* zbits, int8_t* dbg_qx, float* dbg_sx,
+                       cudaStream_t s) {
     const size_t smem = static_cast<size_t>(d) * 4 + static_cast<size_t>(W.TB) * d;
     const int run = select_run(d, kSelThreads);   // d <= 16384: at most 16
     if (run > 16) return PROX_ERR_UNSUPPORTED;
     auto fn = run <= 4 ? input_quant_kernel<4> : (run <= 8 ? input_quant_kernel<8> : input_quant_kernel<16>);
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    return launch_pdl(fn, dim3(1), dim3(kSelThreads), smem, s, x, d, nb, W.TB, k_in,
-                      reinterpret_cast<int*>(ws + W.grows), reinterpret_cast<int*>(ws + W.gcnt),
-                      reinterpret_cast<int*>(ws + W.gq), reinterpret_cast<int8_t*>(ws + W.gqx),
-                      reinterpret_cast<float*>(ws + W.sx),
-                      reinterpret_cast<int*>(ws + W.ghist), dbg_qx, dbg_sx);
+    const int ntiles = (B + W.TB - 1) / W.TB;
+    return launch_pdl(fn, dim3(ntiles), dim3(kSelThreads), smem, s, x, d, B, W.TB,
+                      stage1_width(B, W.TB), k_in, reinterpret_cast<int*>(ws + W.grows),
+                      reinterpret_cast<int*>(ws + W.gcnt), reinterpret_cast<int*>(ws + W.gq),
+                      reinterpret_cast<int8_t*>(ws + W.gqx), reinterpret_cast<float*>(ws + W.sx),
+                      reinterpret_cast<int*>(ws + W.ghist), zbits, F, dbg_qx, dbg_sx);
 }
 
 template <int TB, int CPL>
-static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb,
-                           const Stage1Plan& pl, uint8_t* ws, const WsLayout& W, float* sigma_tile,
+static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, int F, int B,
+                           const Stage1Plan& pl, uint8_t* ws, const WsLayout& W, float* sigma,
                            int32_t* dbg_gate, int32_t* dbg_up, cudaStream_t s) {
     constexpr int NV = 2 * CPL * TB;
     constexpr int TILE = 32 * CPL;
@@ -447,7 +507,7 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
     auto fn = stage1_kernel<TB, CPL>;
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.tiles, pl.S);
+    cfg.gridDim = dim3(pl.tiles, pl.S, (B + TB - 1) / TB);   // z: token tiles
     cfg.blockDim = dim3(kS1Threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -465,21 +525,20 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
         static_cast<const int*>(reinterpret_cast<const int*>(ws + W.grows)),
         static_cast<const int*>(reinterpret_cast<const int*>(ws + W.gq)),
         static_cast<const int8_t*>(reinterpret_cast<const int8_t*>(ws + W.gqx)),
-        static_cast<const float*>(reinterpret_cast<const float*>(ws + W.sx)), pl.gps, pl.S, nb,
-        sigma_tile, reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
+        static_cast<const float*>(reinterpret_cast<const float*>(ws + W.sx)), pl.gps, pl.S, B,
+        sigma, reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
         &reinterpret_cast<Control*>(ws + W.control)->status);
     return err == cudaSuccess ? PROX_OK : cuda_fail(err, "Stage-1 cluster launch");
 }
 
-int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int nb, int k_in,
-                  uint8_t* ws, const WsLayout& W, float* sigma_tile, int32_t* dbg_gate,
-                  int32_t* dbg_up, int sms, cudaStream_t s) {
-    (void)k_in;
-    const int TB = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);
+int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int B, uint8_t* ws,
+                  const WsLayout& W, float* sigma, int32_t* dbg_gate, int32_t* dbg_up, int sms,
+                  cudaStream_t s) {
+    const int TB = stage1_width(B, W.TB);
     const Stage1Plan pl = stage1_plan(d, F, TB, sms);
-    if (TB == 1) return launch_stage1_t<1, 16>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
-    if (TB == 2) return launch_stage1_t<2, 8>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
-    return launch_stage1_t<4, 4>(packed, L, d, F, nb, pl, ws, W, sigma_tile, dbg_gate, dbg_up, s);
+    if (TB == 1) return launch_stage1_t<1, 16>(packed, L, d, F, B, pl, ws, W, sigma, dbg_gate, dbg_up, s);
+    if (TB == 2) return launch_stage1_t<2, 8>(packed, L, d, F, B, pl, ws, W, sigma, dbg_gate, dbg_up, s);
+    return launch_stage1_t<4, 4>(packed, L, d, F, B, pl, ws, W, sigma, dbg_gate, dbg_up, s);
 }
 
 }  // namespace prox

@@ -5,7 +5,7 @@
 // the matching rows of W_down^T contribute to y). With a batch, the selected set is the union
 // U of the tokens' masks and each token keeps only its own channels:
 //     y_b = sum over j in U with j in M_b of SiLU(x_b . Wg[j]) (x_b . Wu[j]) W_down^T[j].
-// For a batch of up to 16 tokens the two gathered projections are dense contractions over
+// For a batch of 2 to 16 tokens the two gathered projections are dense contractions over
 // the batch, so they run as tcgen05 MMAs (bf16 operands, fp32 accumulation in tensor memory).
 //
 // Precision: x and h = SiLU(g) u are fp32 on the CUDA-core path. Here each is split into a
@@ -14,14 +14,20 @@
 // tokens) and the two halves of the accumulator are added in fp32 afterwards. The weights are
 // bf16 already. Products are exact in fp32 and accumulate in fp32.
 //
-// Work split: one CTA per SM owns a contiguous slice of the union (at most kTcListMax
-// channels). Warps 0..3 copy, warp 4 issues the MMAs, warps 5..8 read the accumulators.
-//   Copies: the gathered rows are brought in by 16-byte cp.async copies from 128 threads (eight
-//     per 128-byte row piece, so each warp copy covers four whole pieces), written straight to
-//     their place in the 128-byte-swizzled canonical layout; each thread's copies complete on
-//     the stage's mbarrier (cp.async.mbarrier.arrive.noinc). A TMA tile::gather4 copy of four
-//     128-byte row pieces was measured to stream at only about 1.9 TB/s on this part, so TMA
-//     carries only the activations here.
+// Work split: one CTA per SM owns the selected channels (nonzero words of the batch's channel
+// bitmap) in a contiguous range of about F / P channels (at most kTcListMax). Eight warps
+// copy, the next warp issues the MMAs, the last four read the accumulators.
+//   Copies, two modes chosen per block from the union's density in its window:
+//     tiles (density above 3/4): the whole window of consecutive channels is copied with TMA
+//       2-D tiles of BH rows x 128 bytes, which land in the 128-byte-swizzled canonical layouts
+//       directly; unselected channels get h = 0.
+//     gather: the selected rows are brought in by 16-byte cp.async copies from 256 threads
+//       (eight per 128-byte row piece, so each warp copy covers four whole pieces), written
+//       straight to their place in the same layouts; each thread's copies complete on the
+//       stage's mbarrier (cp.async.mbarrier.arrive.noinc).
+//     Measured on this part: TMA tile::gather4 copies of four 128-byte row pieces stream at
+//     about 1.9 TB/s and the cp.async gather at up to about 4.9 TB/s; whole tiles stream
+//     like any TMA operand load.
 //   Phase A, per M-tile of 128 of the slice's channels: D_gate, D_up [128 x N] accumulate over
 //     d in stages of 64 inputs. The A operand is 128 gathered channel rows x 128 bytes in the
 //     K-major layout; the B operand is the [N x 64] slice of the split activations (one TMA
@@ -30,8 +36,9 @@
 //     the token did not select the channel) and writes the hi/lo pair into the B operand of
 //     phase B (K-major, no swizzle, resident in shared memory for the whole slice).
 //   Phase B, per tile of 128 outputs: D_y [128 x N] = W_down^T[slice, tile]^T . h, with the
-//     W_down^T rows gathered the same way into the MN-major layout (outputs contiguous),
-//     K = the slice's channels in steps of 16.
+//     W_down^T rows copied the same way into the MN-major layout (outputs contiguous; the two
+//     64-output halves 16 KB apart, groups of 8 channels 1 KB apart), K = the slice's
+//     channels in steps of 16.
 //   Epilogue B: y_b = D_y[:, b] + D_y[:, BP + b] is stored as the block's partial output
 //     ypart[block][b][tile]; a fixed-order reduction over blocks follows (bit-reproducible).
 // Every wait is bounded; a wait that runs out records PROX_ERR_TIMEOUT and the roles leave
@@ -47,9 +54,9 @@ namespace prox {
 
 namespace {
 
-constexpr int kTcProducers = 128;           // warps 0..3 copy
-constexpr int kTcMmaWarp = 4;               // warp 4 issues the MMAs, warps 5..8 epilogue
-constexpr int kTcThreads = 288;
+constexpr int kTcProducers = 256;           // warps 0..7 copy
+constexpr int kTcMmaWarp = kTcProducers / 32;   // then one MMA warp, then four epilogue warps
+constexpr int kTcThreads = kTcProducers + 32 + 128;
 constexpr int kTcSlots = 5;                 // ring of stage buffers
 constexpr uint32_t kTcSlotBytes = 36 * 1024;
 constexpr uint32_t kTcUpOff = 16 * 1024;    // phase-A slot: gate rows | up rows | activations
@@ -178,10 +185,10 @@ constexpr int kBarFull = 0, kBarEmpty = kTcSlots, kBarAFull = 2 * kTcSlots,
 
 template <int BP>
 __global__ void __launch_bounds__(kTcThreads, 1)
-stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CUtensorMap tm_x,
-                 int d, int F, int nb, const int32_t* __restrict__ list,
-                 const uint32_t* __restrict__ lbits, const int* __restrict__ count_dev,
-                 int count_host, float* __restrict__ ypart, long long spin, int* status) {
+stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CUtensorMap tm_rows,
+                 const __grid_constant__ CUtensorMap tm_x, int BH, int d, int F, int nb,
+                 const uint32_t* __restrict__ ubits, float* __restrict__ ypart, long long spin,
+                 int* status) {
     constexpr int N = 2 * BP;
     constexpr uint32_t kIdescA = mma_idesc(128, N, 0, 0);
     constexpr uint32_t kIdescB = mma_idesc(128, N, 1, 0);
@@ -193,7 +200,8 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
     int32_t* s_ch = reinterpret_cast<int32_t*>(sbase + SL.ch);
     uint32_t* s_bits = reinterpret_cast<uint32_t*>(sbase + SL.bits);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + SL.bars);
-    uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + SL.misc);   // [0] tmem, [1] issued, [2] consumed
+    // misc: [0] tensor-memory address, [1] stages issued, [2] stages consumed, [3] channels
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + SL.misc);
     const uint32_t slot0 = base + SL.slots, hop = base + SL.hop;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -214,7 +222,12 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
         misc[1] = 0;
         misc[2] = 0;
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_x) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_rows) : "memory");
     }
+    // rows a tile copy does not cover must read as zeros (their h is zero too)
+    for (uint32_t i = tid; i < kTcSlots * kTcSlotBytes / 16; i += kTcThreads)
+        reinterpret_cast<int4*>(sbase + SL.slots)[i] = make_int4(0, 0, 0, 0);
+    fence_smem_async();
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_addr(&misc[0])),
@@ -226,54 +239,74 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
     grid_dep_wait();
     grid_dep_launch();
 
-    // this block's slice of the union
-    const int cnt = list ? *count_dev : count_host;
+    // this block's slice of the union: the selected channels among [c_lo, c_hi)
     const int P = gridDim.x;
-    const int u0 = static_cast<int>(static_cast<long long>(cnt) * blockIdx.x / P);
-    int cb = static_cast<int>(static_cast<long long>(cnt) * (blockIdx.x + 1) / P) - u0;
-    if (cb > kTcListMax || cnt > F) {
-        if (tid == 0) set_status(status, PROX_ERR_BOUNDS);
-        cb = 0;
-    }
-    const int cb16 = (cb + 15) & ~15;
+    const int c_lo = static_cast<int>(static_cast<long long>(F) * blockIdx.x / P);
+    const int c_hi = static_cast<int>(static_cast<long long>(F) * (blockIdx.x + 1) / P);
     const uint32_t all_bits = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
-    for (int i = tid; i < cb16; i += kTcThreads) {
-        int ch = 0;
-        uint32_t bt = 0;
-        if (i < cb) {
-            ch = list ? list[u0 + i] : u0 + i;
-            bt = list ? lbits[u0 + i] : all_bits;
-            if (ch < 0 || ch >= F) {
-                set_status(status, PROX_ERR_BOUNDS);
-                ch = 0;
-                bt = 0;
+    if (warp == 0) {
+        int n = 0;
+        for (int c = c_lo; c < c_hi; c += 32) {
+            const int ch = c + lane;
+            uint32_t bt = 0u;
+            if (ch < c_hi) bt = ubits ? (ubits[ch] & all_bits) : all_bits;
+            const uint32_t m = __ballot_sync(0xffffffffu, bt != 0u);
+            const int pos = n + __popc(m & ((1u << lane) - 1u));
+            if (bt != 0u && pos < kTcListMax) {
+                s_ch[pos] = ch;
+                s_bits[pos] = bt;
             }
+            n += __popc(m);
         }
-        s_ch[i] = ch;
-        s_bits[i] = bt;
+        if (lane == 0) misc[3] = static_cast<uint32_t>(n);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // padding rows repeat the last channel (finite data; their h is zero)
-    if (cb > 0)
-        for (int i = cb + tid; i < cb16; i += kTcThreads) s_ch[i] = s_ch[cb - 1];
+    int cb = static_cast<int>(misc[3]);
+    if (cb > kTcListMax) {
+        if (tid == 0) set_status(status, PROX_ERR_BOUNDS);
+        cb = 0;
+    }
+    // Copy mode: a window whose union density is above 3/4 is copied whole with TMA tiles of
+    // BH consecutive rows (the unselected channels get h = 0); otherwise the selected rows
+    // are gathered by the cp.async threads. M-tile / K-chunk i holds rows_of(i) rows.
+    const int R = c_hi - c_lo;
+    const bool tiles = BH > 0 && cb * 4 > R * 3;
+    const int nmt = tiles ? (R + BH - 1) / BH : (cb + 127) >> 7;
+    auto rows_of = [&](int i) { return tiles ? BH : min(128, cb - i * 128); };
+    if (tiles) {
+        // per-row-slot token bits of the window: slot i * 128 + m is channel c_lo + i * BH + m
+        __syncthreads();
+        for (int j = tid; j < nmt * 128; j += kTcThreads) {
+            const int i = j >> 7, m = j & 127, c = c_lo + i * BH + m;
+            uint32_t bt = 0u;
+            if (m < BH && c < c_hi) bt = ubits ? (ubits[c] & all_bits) : all_bits;
+            s_bits[j] = bt;
+        }
+    } else if (cb > 0) {
+        // padding rows repeat the last channel (finite data; their h is zero)
+        for (int i = cb + tid; i < ((cb + 15) & ~15); i += kTcThreads) {
+            s_ch[i] = s_ch[cb - 1];
+            s_bits[i] = 0u;
+        }
+    }
     __syncthreads();
     const uint32_t tmem = misc[0];
-
-    const int nmt = (cb + 127) >> 7;       // M-tiles of phase A, K-chunks of phase B
     const int nka = d >> 6;                // phase-A stages per M-tile
     const int ntile = d >> 7;              // phase-B output tiles
 
     if (cb > 0 && tid < kTcProducers) {
         // ---------------------------------------------------------------- copies
-        // thread p copies 16-byte chunk (p % 8) of row pieces p / 8, p / 8 + 16, ...
+        // gather mode: thread p copies 16-byte chunk (p % 8) of row pieces p / 8,
+        // p / 8 + kTcProducers / 8, ...; tile mode: thread 0 issues the TMA tile copies.
+        // Every producer thread arrives once per stage.
         const size_t pitch = static_cast<size_t>(3) * d;   // elements per packed channel run
         const int chunk = tid & 7;
         uint32_t it = 0;
         bool ok = true;
         for (int mt = 0; ok && mt < nmt; ++mt) {
-            const int rows = min(128, cb - mt * 128);
+            const int rows = rows_of(mt);
             for (int kc = 0; kc < nka; ++kc, ++it) {
                 const int slot = it % kTcSlots;
                 if (it >= kTcSlots &&
@@ -282,25 +315,33 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                     break;
                 }
                 const uint32_t sb = slot0 + slot * kTcSlotBytes;
+                uint64_t* fb = &bars[kBarFull + slot];
                 if (tid == 0) {
-                    mbar_arrive_expect_tx(&bars[kBarFull + slot], N * 128u);
-                    tma_tile_2d(sb + kTcXOff, &tm_x, kc * 64, 0, &bars[kBarFull + slot]);
+                    mbar_arrive_expect_tx(fb, N * 128u + (tiles ? 256u * BH : 0u));
+                    tma_tile_2d(sb + kTcXOff, &tm_x, kc * 64, 0, fb);
+                    if (tiles) {
+                        const int row = c_lo + mt * BH;
+                        tma_tile_2d(sb, &tm_rows, kc * 64, row, fb);
+                        tma_tile_2d(sb + kTcUpOff, &tm_rows, d + kc * 64, row, fb);
+                    }
                 }
-                // gate pieces (proj 0) then up pieces (proj 1) of the M-tile's rows
-                for (int i = tid >> 3; i < 2 * rows; i += kTcProducers / 8) {
-                    const int proj = i >= rows, r = i - proj * rows;
-                    const uint16_t* src = rows_g + s_ch[mt * 128 + r] * pitch + proj * d +
-                                          kc * 64 + chunk * 8;
-                    const uint32_t dst = sb + proj * kTcUpOff + (r >> 3) * 1024 + (r & 7) * 128 +
-                                         ((chunk ^ (r & 7)) << 4);
-                    cp_async16(dst, src);
+                if (!tiles) {
+                    // gate pieces (proj 0) then up pieces (proj 1) of the M-tile's rows
+                    for (int i = tid >> 3; i < 2 * rows; i += kTcProducers / 8) {
+                        const int proj = i >= rows, r = i - proj * rows;
+                        const uint16_t* src = rows_g + s_ch[mt * 128 + r] * pitch + proj * d +
+                                              kc * 64 + chunk * 8;
+                        const uint32_t dst = sb + proj * kTcUpOff + (r >> 3) * 1024 +
+                                             (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+                        cp_async16(dst, src);
+                    }
                 }
-                cp_async_arrive(&bars[kBarFull + slot]);
+                cp_async_arrive(fb);
             }
         }
         for (int t = 0; ok && t < ntile; ++t) {
             for (int kc = 0; kc < nmt; ++kc, ++it) {
-                const int rows = min(128, cb - kc * 128);
+                const int rows = rows_of(kc);
                 const int r16 = (rows + 15) & ~15;
                 const int slot = it % kTcSlots;
                 if (it >= kTcSlots &&
@@ -309,18 +350,28 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                     break;
                 }
                 const uint32_t sb = slot0 + slot * kTcSlotBytes;
-                if (tid == 0) mbar_arrive_expect_tx(&bars[kBarFull + slot], 0u);
-                // W_down^T row pieces of 64 outputs: MN-major atoms (8 channels x 128 bytes),
-                // atom (channel group, output half) at group * 2048 + half * 1024
-                for (int i = tid >> 3; i < 2 * r16; i += kTcProducers / 8) {
-                    const int half = i & 1, r = i >> 1;
-                    const uint16_t* src = rows_g + s_ch[kc * 128 + r] * pitch + 2 * d + t * 128 +
-                                          half * 64 + chunk * 8;
-                    const uint32_t dst = sb + (r >> 3) * 2048 + half * 1024 + (r & 7) * 128 +
-                                         ((chunk ^ (r & 7)) << 4);
-                    cp_async16(dst, src);
+                uint64_t* fb = &bars[kBarFull + slot];
+                // W_down^T row pieces of 64 outputs in MN-major atoms (8 channels x 128 bytes):
+                // output half h at h * 16 KB, channel group g at g * 1 KB
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(fb, tiles ? 256u * BH : 0u);
+                    if (tiles) {
+                        const int row = c_lo + kc * BH;
+                        tma_tile_2d(sb, &tm_rows, 2 * d + t * 128, row, fb);
+                        tma_tile_2d(sb + kTcUpOff, &tm_rows, 2 * d + t * 128 + 64, row, fb);
+                    }
                 }
-                cp_async_arrive(&bars[kBarFull + slot]);
+                if (!tiles) {
+                    for (int i = tid >> 3; i < 2 * r16; i += kTcProducers / 8) {
+                        const int half = i & 1, r = i >> 1;
+                        const uint16_t* src = rows_g + s_ch[kc * 128 + r] * pitch + 2 * d +
+                                              t * 128 + half * 64 + chunk * 8;
+                        const uint32_t dst = sb + half * kTcUpOff + (r >> 3) * 1024 +
+                                             (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+                        cp_async16(dst, src);
+                    }
+                }
+                cp_async_arrive(fb);
             }
         }
         cp_async_wait_all();
@@ -369,8 +420,7 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
             tc_fence_after();
             const uint32_t dy = tmem + 128 + buf * 32;
             for (int kc = 0; kc < nmt; ++kc, ++it) {
-                const int rows = min(128, cb - kc * 128);
-                const int r16 = (rows + 15) & ~15;
+                const int r16 = (rows_of(kc) + 15) & ~15;
                 const int slot = it % kTcSlots;
                 if (!mbar_wait(&bars[kBarFull + slot], (it / kTcSlots) & 1, spin, status)) {
                     ok = false;
@@ -380,7 +430,7 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                 tc_fence_after();
                 const uint32_t sb = slot0 + slot * kTcSlotBytes;
                 for (int ks = 0; ks < r16 / 16; ++ks) {
-                    const uint64_t a = smem_desc(sb + ks * 4096, 1024, 2048, kLayoutSw128);
+                    const uint64_t a = smem_desc(sb + ks * 2048, kTcUpOff, 1024, kLayoutSw128);
                     const uint64_t b =
                         smem_desc(hop + (kc * 16 + ks * 2) * 128, 128, kTcHSbo, kLayoutNone);
                     mma_bf16(dy, a, b, kIdescB, (kc | ks) != 0);
@@ -416,8 +466,8 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kBarAEmpty + buf]);
             const int cl = mt * 128 + m;
-            if (cl < cb16) {
-                const uint32_t bt = cl < cb ? s_bits[cl] : 0u;
+            if (m < ((rows_of(mt) + 15) & ~15)) {
+                const uint32_t bt = s_bits[cl];
                 unsigned char* hp = sbase + SL.hop + (cl >> 3) * 128 + (cl & 7) * 2;
 #pragma unroll
                 for (int b = 0; b < BP; ++b) {
@@ -526,14 +576,14 @@ int encode_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, 
 }
 
 template <int BP>
-int launch_tc_t(const uint16_t* rows, const CUtensorMap& tm_x, int d, int F, int nb,
-                const int32_t* list, const uint32_t* lbits, const int* count_dev, int count_host,
-                float* ypart, int P, int* status, cudaStream_t s) {
+int launch_tc_t(const uint16_t* rows, const CUtensorMap& tm_rows, const CUtensorMap& tm_x, int BH,
+                int d, int F, int nb, const uint32_t* bits, float* ypart, int P, int* status,
+                cudaStream_t s) {
     const size_t smem = tc_smem_layout(BP).total;
     auto fn = stage2_tc_kernel<BP>;
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    return launch_pdl(fn, dim3(P), dim3(kTcThreads), smem, s, rows, tm_x, d, F, nb, list, lbits,
-                      count_dev, count_host, ypart, kDefaultSpinCycles, status);
+    return launch_pdl(fn, dim3(P), dim3(kTcThreads), smem, s, rows, tm_rows, tm_x, BH, d, F, nb,
+                      bits, ypart, kDefaultSpinCycles, status);
 }
 
 }  // namespace
@@ -544,9 +594,8 @@ bool stage2_tc_supported(int d, int F, int nb, int sms) {
 }
 
 int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F, const float* x,
-                     int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
-                     int count_host, float* y, uint8_t* ws, const WsLayout& W, int sms,
-                     cudaStream_t s) {
+                     int nb, const uint32_t* bits, float* y, uint8_t* ws, const WsLayout& W,
+                     int sms, cudaStream_t s) {
     if (!stage2_tc_supported(d, F, nb, sms) || W.BPtc < nb) return PROX_ERR_UNSUPPORTED;
     const int BP = W.BPtc;
     const int P = tc_blocks(F, sms);
@@ -554,16 +603,22 @@ int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F,
     float* ypart = reinterpret_cast<float*>(ws + W.ypart);
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
     const uint16_t* rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
-    CUtensorMap tm_x;
+    // tile copies: a block's window of at most ceil(F / P) channels in nmt tiles of BH rows
+    const int rmax = (F + P - 1) / P;
+    const int nmt = (rmax + 127) / 128;
+    const int BH = (rmax + nmt - 1) / nmt;
+    CUtensorMap tm_rows, tm_x;
+    if (encode_map(&tm_rows, rows, static_cast<uint64_t>(3) * d, F, static_cast<uint64_t>(6) * d,
+                   BH) != PROX_OK)
+        return PROX_ERR_CUDA;
     if (encode_map(&tm_x, xhl, d, 2 * BP, static_cast<uint64_t>(2) * d, 2 * BP) != PROX_OK)
         return PROX_ERR_CUDA;
     const int total = BP * d;
     int rc = launch_pdl(split_x_kernel, dim3((total + 1023) / 1024), dim3(256), 0, s, x, nb, d, BP,
                         xhl);
     if (rc != PROX_OK) return rc;
-    rc = BP == 16 ? launch_tc_t<16>(rows, tm_x, d, F, nb, list, lbits, count_dev, count_host,
-                                    ypart, P, status, s)
-                  : PROX_ERR_UNSUPPORTED;
+    rc = BP == 16 ? launch_tc_t<16>(rows, tm_rows, tm_x, BH, d, F, nb, bits, ypart, P, status, s)
+                  : launch_tc_t<8>(rows, tm_rows, tm_x, BH, d, F, nb, bits, ypart, P, status, s);
     if (rc != PROX_OK) return rc;
     return launch_reduce_partials(ypart, P, BP, d, nb, y, s);
 }
