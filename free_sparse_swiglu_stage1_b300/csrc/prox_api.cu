@@ -151,10 +151,18 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
         }
         return PROX_OK;
     }
-    PROX_TRY(launch_input_quant(x, d, F, B, k_in, ws, W, tc ? ubits : nullptr,
+    // a batch larger than one token tile runs its proxy GEMV on the tensor cores (over the
+    // dense activation codes); within one tile the CUDA-core kernel reads only the tile's
+    // union of kept inputs, which measured faster
+    const bool s1tc = B > W.TB && W.BPtc > 0 && stage1_tc_supported(d, F, B, sms);
+    PROX_TRY(launch_input_quant(x, d, F, B, k_in, ws, W, tc ? ubits : nullptr, s1tc,
                                 dbg ? dbg->qx : nullptr, dbg ? dbg->sx : nullptr, s));
-    PROX_TRY(launch_stage1(packed, L, d, F, B, ws, W, sigma, dbg ? dbg->acc_gate : nullptr,
-                           dbg ? dbg->acc_up : nullptr, sms, s));
+    if (s1tc)
+        PROX_TRY(launch_stage1_tc(packed, L, d, F, B, ws, W, sigma, dbg ? dbg->acc_gate : nullptr,
+                                  dbg ? dbg->acc_up : nullptr, sms, s));
+    else
+        PROX_TRY(launch_stage1(packed, L, d, F, B, ws, W, sigma, dbg ? dbg->acc_gate : nullptr,
+                               dbg ? dbg->acc_up : nullptr, sms, s));
     if (dbg) return PROX_OK;
     const int* ghist = reinterpret_cast<const int*>(ws + W.ghist);
     if (g_fused_sel && y && !idx_out && B == 1 && stage2_select_supported(d, F)) {

@@ -134,14 +134,17 @@ __device__ __forceinline__ DF df_add(DF a, DF b) {
 // (p * q) * n as a double-float, with p, q binary32 and n an integer below 2^24 in size.
 // p*q is split exactly by FMA; the (hi part) * n product too; the low part's product is
 // rounded once, which is far below the precision the salience needs.
-__device__ __forceinline__ DF df_scaled_int(float p, float q, int n) {
+// The same with the integer given as a float that holds it exactly.
+__device__ __forceinline__ DF df_scaled(float p, float q, float nf) {
     const float ph = __fmul_rn(p, q);
     const float pl = __fmaf_rn(p, q, -ph);
-    const float nf = static_cast<float>(n);
     const float th = __fmul_rn(ph, nf);
     const float tl = __fmaf_rn(ph, nf, -th) + __fmul_rn(pl, nf);
     const float hi = th + tl;
     return DF{hi, tl - (hi - th)};
+}
+__device__ __forceinline__ DF df_scaled_int(float p, float q, int n) {
+    return df_scaled(p, q, static_cast<float>(n));
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }

@@ -89,8 +89,8 @@ inline int tc_blocks(int F, int sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, sigma, idx, ulist, ubits, xhl,
-        ypart, total;
+    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, qxh, sigma, idx, ulist, ubits,
+        xhl, ypart, total;
     int TB, P, BPtc;
 };
 
@@ -98,7 +98,9 @@ struct WsLayout {
 // inputs: grows [G][128] (the group's kept inputs, ascending, padded to a multiple of 4 with
 // copies of the last), gcnt [G] (padded counts), gq [G + 1] (quad offsets: exclusive sums of
 // gcnt / 4), gqx [TB][G][128] int8 codes, sx [TB][G] scales, ghist [TB][2048]; each of these
-// is repeated for every tile of TB tokens. ubits [F] holds the batch union's token bits
+// is repeated for every tile of TB tokens. For a batch (2+ tokens), qxh [16][d] holds every
+// token's activation codes as f16 (0 where dropped; rows past the batch 0) for the
+// tensor-core Stage 1. ubits [F] holds the batch union's token bits
 // (compacted with ulist on the CUDA-core path, one word per channel on the tensor-core path).
 inline WsLayout ws_layout(int d, int F, int B, int sms) {
     WsLayout W;
@@ -118,6 +120,7 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     W.gq = take(nt * (G + 1) * 4);
     W.sx = take(nt * W.TB * G * 4);
     W.ghist = take(nt * W.TB * 2048 * 4);
+    W.qxh = take(W.BPtc > 0 ? static_cast<size_t>(kTcMaxTokens) * d * 2 : 0);
     W.sigma = take(static_cast<size_t>(B) * F * 4);
     W.idx = take(static_cast<size_t>(B) * F * 4);
     W.ulist = take(static_cast<size_t>(F) * 4);
@@ -175,15 +178,24 @@ int launch_pack(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_
 // Input selection + activation quantization (Stage 1 inputs) for all B tokens, one block
 // per tile of W.TB tokens. Also clears the tiles' salience histograms (ws + W.ghist) that
 // Stage 1 fills for the top-k, and zbits [F] (if not null) for the top-k's channel bitmap.
+// dense_codes: also write every token's codes as f16 into qxh (for the tensor-core Stage 1).
 int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* ws,
-                       const WsLayout& W, uint32_t* zbits, int8_t* dbg_qx, float* dbg_sx,
-                       cudaStream_t s);
+                       const WsLayout& W, uint32_t* zbits, bool dense_codes, int8_t* dbg_qx,
+                       float* dbg_sx, cudaStream_t s);
 
 // Stage-1 proxy projections + salience for all B tokens (grid z: token tiles);
 // sigma [B][F].
 int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int B, uint8_t* ws,
                   const WsLayout& W, float* sigma, int32_t* dbg_gate, int32_t* dbg_up, int sms,
                   cudaStream_t s);
+
+// Stage 1 of a batch (2..16 tokens) on the tensor cores: the same exact per-group integers
+// from f16 MMAs over the dense activation codes qxh, the same double-float scaling; sigma [B][F]
+// and the top-k histograms. Needs input_quant to have written qxh.
+bool stage1_tc_supported(int d, int F, int B, int sms);
+int launch_stage1_tc(const uint8_t* packed, const PackedLayout& L, int d, int F, int B,
+                     uint8_t* ws, const WsLayout& W, float* sigma, int32_t* dbg_gate,
+                     int32_t* dbg_up, int sms, cudaStream_t s);
 
 // Per-token top-k of the salience [B][F] -> ascending channel indices (row stride k), one
 // block per token. ghist, if not null, holds per token the 2048-bin histogram of the

@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(kSelThreads)
 input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, int k_in,
                    int* __restrict__ grows, int* __restrict__ gcnt, int* __restrict__ gq,
                    int8_t* __restrict__ gqx, float* __restrict__ sx_ws, int* __restrict__ ghist,
-                   uint32_t* __restrict__ zbits, int F, int8_t* __restrict__ dbg_qx,
-                   float* __restrict__ dbg_sx) {
+                   uint32_t* __restrict__ zbits, int F, uint16_t* __restrict__ qxh,
+                   int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                 // [d]
     int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);                   // [TB][d]
@@ -82,6 +82,8 @@ input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, i
         reinterpret_cast<int4*>(ghist)[i] = make_int4(0, 0, 0, 0);
     if (zbits && z == 0)   // the batch's channel bitmap, filled by the top-k
         for (int i = tid; i < F; i += NT) zbits[i] = 0u;
+    if (qxh && z == 0)     // dense f16 codes: rows past the batch stay zero
+        for (int i = B * d + tid; i < kTcMaxTokens * d; i += NT) qxh[i] = 0;
     uint64_t any = 0ull;
     for (int b = 0; b < nb; ++b) {
         float xv[RUN];
@@ -125,6 +127,12 @@ input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, i
             qw[e >> 2] |= qb << (8 * (e & 3));
         }
         if (active) {
+            if (qxh) {
+                uint16_t* qh = qxh + static_cast<size_t>(t0 + b) * d + lo;
+#pragma unroll
+                for (int e = 0; e < RUN; ++e)
+                    qh[e] = __half_as_ushort(__int2half_rn(static_cast<int>(static_cast<int8_t>(qw[e >> 2] >> (8 * (e & 3))))));
+            }
 #pragma unroll
             for (int e4 = 0; e4 < RUN / 4; ++e4) {
                 *reinterpret_cast<uint32_t*>(qx8 + b * d + lo + e4 * 4) = qw[e4];
@@ -479,8 +487,9 @@ stage1_kernel(const uint8_t* __restrict__ codes, const uint32_t* __restrict__ sc
 }
 
 int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* ws,
-                       const WsLayout& W, uint32_t* zbits, int8_t* dbg_qx, float* dbg_sx,
-                       cudaStream_t s) {
+                       const WsLayout& W, uint32_t* zbits, bool dense_codes, int8_t* dbg_qx,
+                       float* dbg_sx, cudaStream_t s) {
+    if (dense_codes && (W.BPtc == 0 || B > kTcMaxTokens)) return PROX_ERR_UNSUPPORTED;
     const size_t smem = static_cast<size_t>(d) * 4 + static_cast<size_t>(W.TB) * d;
     const int run = select_run(d, kSelThreads);   // d <= 16384: at most 16
     if (run > 16) return PROX_ERR_UNSUPPORTED;
@@ -491,7 +500,9 @@ int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* w
                       stage1_width(B, W.TB), k_in, reinterpret_cast<int*>(ws + W.grows),
                       reinterpret_cast<int*>(ws + W.gcnt), reinterpret_cast<int*>(ws + W.gq),
                       reinterpret_cast<int8_t*>(ws + W.gqx), reinterpret_cast<float*>(ws + W.sx),
-                      reinterpret_cast<int*>(ws + W.ghist), zbits, F, dbg_qx, dbg_sx);
+                      reinterpret_cast<int*>(ws + W.ghist), zbits, F,
+                      dense_codes ? reinterpret_cast<uint16_t*>(ws + W.qxh) : nullptr, dbg_qx,
+                      dbg_sx);
 }
 
 template <int TB, int CPL>

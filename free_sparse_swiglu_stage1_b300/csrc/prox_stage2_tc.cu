@@ -43,12 +43,7 @@
 //     ypart[block][b][tile]; a fixed-order reduction over blocks follows (bit-reproducible).
 // Every wait is bounded; a wait that runs out records PROX_ERR_TIMEOUT and the roles leave
 // their loops; copies still in flight are drained (bounded) and tensor memory is freed.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "prox_kernels.cuh"
+#include "prox_tc.cuh"
 
 namespace prox {
 
@@ -63,93 +58,6 @@ constexpr uint32_t kTcUpOff = 16 * 1024;    // phase-A slot: gate rows | up rows
 constexpr uint32_t kTcXOff = 32 * 1024;
 constexpr uint32_t kTcTmemCols = 256;       // A accumulators 2 x 64 columns, D_y 2 x 32
 constexpr uint32_t kTcHSbo = kTcListMax * 16;   // h operand: bytes between 8-row groups
-
-// ------------------------------------------------------------------ tcgen05 / TMA wrappers
-// 16-byte asynchronous copy global -> shared (L2 only, 256-byte L2 fetch granularity).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src)
-                 : "memory");
-}
-// The mbarrier counts one arrival once all of this thread's earlier cp.async copies are done.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_tile_2d(uint32_t dst, const CUtensorMap* tm, int c0, int c1,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(tm), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: start address, leading and stride byte offsets (16-byte
-// units), descriptor version 1, layout (0 = no swizzle, 2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t layout) {
-    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) |
-           (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
-           (static_cast<uint64_t>(layout) << 61);
-}
-constexpr uint32_t kLayoutNone = 0, kLayoutSw128 = 2;
-
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A/B major-ness
-// (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Orders this thread's ordinary shared-memory stores before later tensor-core reads.
-__device__ __forceinline__ void fence_smem_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-        "%11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -190,8 +98,8 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                  const uint32_t* __restrict__ ubits, float* __restrict__ ypart, long long spin,
                  int* status) {
     constexpr int N = 2 * BP;
-    constexpr uint32_t kIdescA = mma_idesc(128, N, 0, 0);
-    constexpr uint32_t kIdescB = mma_idesc(128, N, 1, 0);
+    constexpr uint32_t kIdescA = mma_idesc(128, N, 0, 0, kFmtBf16);
+    constexpr uint32_t kIdescB = mma_idesc(128, N, 1, 0, kFmtBf16);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const TcSmem SL = tc_smem_layout(BP);
     const uint32_t raw = smem_addr(smem_raw);
@@ -229,11 +137,7 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
         reinterpret_cast<int4*>(sbase + SL.slots)[i] = make_int4(0, 0, 0, 0);
     fence_smem_async();
     if (warp == kTcMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr(&misc[0])),
-                     "r"(kTcTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc(&misc[0], kTcTmemCols);
     }
 
     grid_dep_wait();
@@ -401,8 +305,8 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t bx = smem_desc(sb + kTcXOff + ks * 32, 16, 1024, kLayoutSw128);
                     const uint32_t acc = (kc | ks) != 0;
-                    mma_bf16(dg, smem_desc(sb + ks * 32, 16, 1024, kLayoutSw128), bx, kIdescA, acc);
-                    mma_bf16(du, smem_desc(sb + kTcUpOff + ks * 32, 16, 1024, kLayoutSw128), bx,
+                    mma_f16(dg, smem_desc(sb + ks * 32, 16, 1024, kLayoutSw128), bx, kIdescA, acc);
+                    mma_f16(du, smem_desc(sb + kTcUpOff + ks * 32, 16, 1024, kLayoutSw128), bx,
                              kIdescA, acc);
                 }
                 mma_commit(&bars[kBarEmpty + slot]);
@@ -433,7 +337,7 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
                     const uint64_t a = smem_desc(sb + ks * 2048, kTcUpOff, 1024, kLayoutSw128);
                     const uint64_t b =
                         smem_desc(hop + (kc * 16 + ks * 2) * 128, 128, kTcHSbo, kLayoutNone);
-                    mma_bf16(dy, a, b, kIdescB, (kc | ks) != 0);
+                    mma_f16(dy, a, b, kIdescB, (kc | ks) != 0);
                 }
                 mma_commit(&bars[kBarEmpty + slot]);
             }
@@ -522,9 +426,7 @@ stage2_tc_kernel(const uint16_t* __restrict__ rows_g, const __grid_constant__ CU
     __syncthreads();
     if (warp == kTcMmaWarp) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTcTmemCols)
-                     : "memory");
+        tmem_free(tmem, kTcTmemCols);
     }
 }
 
@@ -544,37 +446,6 @@ split_x_kernel(const float* __restrict__ x, int nb, int d, int BP, uint16_t* __r
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D bf16 tensor map with the 128-byte swizzle: rows x cols elements, row pitch in bytes,
-// box of box_rows x 64 elements.
-int encode_map(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch,
-               uint32_t box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return cuda_fail(cudaErrorNotSupported, "looking up cuTensorMapEncodeTiled");
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {pitch};
-    const cuuint32_t box[2] = {64, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? PROX_OK : cuda_fail(cudaErrorInvalidValue, "encoding a tensor map");
-}
-
 template <int BP>
 int launch_tc_t(const uint16_t* rows, const CUtensorMap& tm_rows, const CUtensorMap& tm_x, int BH,
                 int d, int F, int nb, const uint32_t* bits, float* ypart, int P, int* status,
@@ -608,10 +479,11 @@ int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F,
     const int nmt = (rmax + 127) / 128;
     const int BH = (rmax + nmt - 1) / nmt;
     CUtensorMap tm_rows, tm_x;
-    if (encode_map(&tm_rows, rows, static_cast<uint64_t>(3) * d, F, static_cast<uint64_t>(6) * d,
-                   BH) != PROX_OK)
+    if (encode_map_2d(&tm_rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rows, static_cast<uint64_t>(3) * d,
+                      F, static_cast<uint64_t>(6) * d, 64, BH, CU_TENSOR_MAP_SWIZZLE_128B) != PROX_OK)
         return PROX_ERR_CUDA;
-    if (encode_map(&tm_x, xhl, d, 2 * BP, static_cast<uint64_t>(2) * d, 2 * BP) != PROX_OK)
+    if (encode_map_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhl, d, 2 * BP,
+                      static_cast<uint64_t>(2) * d, 64, 2 * BP, CU_TENSOR_MAP_SWIZZLE_128B) != PROX_OK)
         return PROX_ERR_CUDA;
     const int total = BP * d;
     int rc = launch_pdl(split_x_kernel, dim3((total + 1023) / 1024), dim3(256), 0, s, x, nb, d, BP,
