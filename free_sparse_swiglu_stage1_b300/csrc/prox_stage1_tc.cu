@@ -18,9 +18,10 @@
 //                 and the activation tile [16 tokens][64 inputs] (f16, 128-byte swizzle);
 //   warps 1..8    unpack the nibbles into two f16 A operands (gate, up) in the MN-major
 //                 128-byte-swizzled layout (channels contiguous), 16 codes per thread-copy;
-//   warp 9        MMAs D_gate, D_up [128 channels x 16 tokens] += A . qx^T (K = 64 per stage);
-//                 the group's accumulators alternate between two tensor-memory buffers;
-//   warps 10..17  per group, read the exact integers of their channel (one TMEM lane per
+//   warps 9, 10   MMAs D_gate, D_up [128 channels x 16 tokens] += A . qx^T (K = 64 per stage),
+//                 one issuing thread per projection; the group's accumulators alternate between
+//                 two tensor-memory buffers;
+//   warps 11..18  per group, read the exact integers of their channel (one TMEM lane per
 //                 thread; two warps per lane quarter, 8 tokens each), scale them by sx sw into
 //                 double-float sums (the same arithmetic as the CUDA-core kernel, groups in
 //                 ascending order); after the last group write the salience and count its top
@@ -33,9 +34,10 @@ namespace prox {
 namespace {
 
 constexpr int kUnpackers = 256;                      // warps 1..8
-constexpr int kMmaWarp = 9;
-constexpr int kEpilogue = 256;                       // warps 10..17: two per TMEM lane quarter
-constexpr int kThreads = 32 + kUnpackers + 32 + kEpilogue;   // 576
+constexpr int kMmaWarp = 9;                          // gate MMAs (and tensor memory)
+constexpr int kMmaWarpUp = 10;                       // up MMAs
+constexpr int kEpilogue = 256;                       // warps 11..18: two per TMEM lane quarter
+constexpr int kThreads = 32 + kUnpackers + 64 + kEpilogue;   // 608
 constexpr int kCodeSlots = 6;
 constexpr uint32_t kCodeBytes = 64 * 128;            // 64 inputs x 128 channels
 constexpr uint32_t kQxBytes = 16 * 128;              // 16 tokens x 64 inputs, f16
@@ -50,7 +52,7 @@ constexpr int kTokens = 16;
 // barrier indices
 constexpr int kCFull = 0, kCEmpty = kCodeSlots, kAFull = 2 * kCodeSlots,
               kAEmpty = kAFull + kASlots, kDFull = kAEmpty + kASlots, kDEmpty = kDFull + 2,
-              kDone = kDEmpty + 2, kNumBars = kDone + 1;
+              kDone = kDEmpty + 2, kNumBars = kDone + 2;
 
 struct S1Smem {
     uint32_t code, a, sx, bars, misc, total;
@@ -118,17 +120,17 @@ stage1_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     if (tid == 0) {
         for (int i = 0; i < kCodeSlots; ++i) {
             mbar_init(&bars[kCFull + i], 1);
-            mbar_init(&bars[kCEmpty + i], kUnpackers / 32 + 1);
+            mbar_init(&bars[kCEmpty + i], kUnpackers / 32 + 2);
         }
         for (int i = 0; i < kASlots; ++i) {
             mbar_init(&bars[kAFull + i], kUnpackers / 32);
-            mbar_init(&bars[kAEmpty + i], 1);
+            mbar_init(&bars[kAEmpty + i], 2);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars[kDFull + i], 1);
+            mbar_init(&bars[kDFull + i], 2);
             mbar_init(&bars[kDEmpty + i], kEpilogue / 32);
+            mbar_init(&bars[kDone + i], 1);
         }
-        mbar_init(&bars[kDone], 1);
         mbar_init_fence();
         misc[1] = 0;
         misc[2] = 0;
@@ -200,8 +202,10 @@ stage1_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
                 mbar_arrive(&bars[kCEmpty + c]);
             }
         }
-    } else if (total > 0 && warp == kMmaWarp && lane == 0) {
+    } else if (total > 0 && (warp == kMmaWarp || warp == kMmaWarpUp) && lane == 0) {
         // ---------------------------------------------------------------- MMA issue
+        // one thread issues the gate MMAs, another the up MMAs (separate accumulators)
+        const int proj = warp == kMmaWarpUp;
         int s = 0;
         bool ok = true;
         for (; ok && s < total; ++s) {
@@ -223,24 +227,21 @@ stage1_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t bq = smem_desc(qs + ks * 32, 16, 1024, kLayoutSw128);
-                const uint32_t acc = (h | ks) != 0;
-                mma_f16(tmem + buf * 32, smem_desc(as + ks * 2048, 8192, 1024, kLayoutSw128), bq,
-                        kIdesc, acc);
-                mma_f16(tmem + buf * 32 + 16,
-                        smem_desc(as + kAProj + ks * 2048, 8192, 1024, kLayoutSw128), bq, kIdesc,
-                        acc);
+                mma_f16(tmem + buf * 32 + proj * 16,
+                        smem_desc(as + proj * kAProj + ks * 2048, 8192, 1024, kLayoutSw128), bq,
+                        kIdesc, (h | ks) != 0);
             }
             mma_commit(&bars[kAEmpty + a]);
             mma_commit(&bars[kCEmpty + c]);
             if (h == 1) mma_commit(&bars[kDFull + buf]);
         }
-        misc[2] = s;
-        mma_commit(&bars[kDone]);
-        mbar_wait(&bars[kDone], 0, spin, status);
-    } else if (total > 0 && warp > kMmaWarp) {
+        if (proj == 0) misc[2] = s;
+        mma_commit(&bars[kDone + proj]);
+        mbar_wait(&bars[kDone + proj], 0, spin, status);
+    } else if (total > 0 && warp > kMmaWarpUp) {
         // ---------------------------------------------------------------- scale and combine
         const int q = warp & 3;
-        const int t0 = ((warp - kMmaWarp - 1) >> 2) * 8;   // this warp's 8 tokens
+        const int t0 = ((warp - kMmaWarpUp - 1) >> 2) * 8;   // this warp's 8 tokens
         const int m = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         bool ok = true;
@@ -262,8 +263,8 @@ stage1_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
                 }
                 tc_fence_after();
                 float vg[8], vu[8];
-                tmem_ld8(tmem + lane_off + buf * 32 + t0, vg);
-                tmem_ld8(tmem + lane_off + buf * 32 + 16 + t0, vu);
+                tmem_ld8x2(tmem + lane_off + buf * 32 + t0, tmem + lane_off + buf * 32 + 16 + t0,
+                           vg, vu);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kDEmpty + buf]);

@@ -42,7 +42,9 @@ def test_pack_bitwise(layer):
     np.testing.assert_array_equal(dec["rows"][:, 2, :], bits(layer.mats["w_down"]).T)
 
 
-@pytest.mark.parametrize("batch,s_in", [(1, 0.5), (3, 0.5), (2, 0.0), (1, 0.9)])
+# batches past one token tile (4 tokens at these widths) take the tensor-core Stage 1
+@pytest.mark.parametrize("batch,s_in", [(1, 0.5), (3, 0.5), (2, 0.0), (1, 0.9), (6, 0.5),
+                                        (16, 0.3)])
 def test_stage1_integers_bitexact(layer, batch, s_in):
     ws = ws_for(layer, batch)
     x = _tokens(batch, layer.d, seed=batch * 7 + int(s_in * 10))
