@@ -94,12 +94,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) from global memory into L2 without
-// waiting; later copies of the same bytes then come from L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch: wait for the previous grid's results / let the next grid
 // start its prologue. Both are no-ops when the launch carried no such dependency.
 __device__ __forceinline__ void grid_dep_wait() {

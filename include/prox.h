@@ -117,9 +117,11 @@ int prox_build_mask(const prox_packed* w, const float* x, int batch,
 
 /* Stage 2 alone, for a given mask (technical summary, Stage 2 "Exact Projections" and
  * "Final Output"): for each token b, y_b = sum over j in idx[b] of
- * SiLU(W_gate[j,:] . x_b) * (W_up[j,:] . x_b) * W_down[:, j], with fp32 activations,
- * bf16 weights and fp32 accumulation; the cross-block sum runs in a fixed order, so the
- * result is bit-reproducible on a given device.
+ * SiLU(W_gate[j,:] . x_b) * (W_up[j,:] . x_b) * W_down[:, j], with bf16 weights and fp32
+ * accumulation. One token runs on the CUDA cores with fp32 activations; a batch of 2 to 16
+ * runs once over the union of its masks on the tensor cores, with x and SiLU(g) * u each
+ * entered as a pair of bf16 values hi + lo (about 17 significant bits). The cross-block sum
+ * runs in a fixed order, so the result is bit-reproducible on a given device.
  *   x   [batch][d_model] fp32 device;  idx [batch][k] int32 device, each row strictly
  *   ascending in [0, d_ff);  y [batch][d_model] fp32 device (written). 1 <= k <= d_ff. */
 int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx,
@@ -147,8 +149,10 @@ int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch,
  * one: for example a serving runtime that has already reserved all device memory for its
  * own pool, or a latency-critical loop that cannot afford the implicit synchronization of
  * cudaMalloc. The pages have no counterpart to this call; it only changes where the
- * scratch lives, not what is computed. Arguments and result are those of prox_sparse_ffn
- * (same kernels, same bits).
+ * scratch lives, not what is computed. Arguments are those of prox_sparse_ffn. For one token
+ * it runs the same kernels (same bits); a batch runs the CUDA-core Stage 2 in token tiles
+ * over each tile's union (fp32 activations), which agrees with prox_sparse_ffn within the
+ * Stage-2 tolerance.
  *   Scratch: a fixed array of PROX_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, held
  *   by every GPU that loads the library until the process exits. A call needs
  *   256 + 8*d_ff + SMs * tile * d_model * 4 bytes (rounded to 256-byte pieces), where tile
@@ -201,8 +205,9 @@ int prox_debug_stage1(const prox_packed* w, const float* x, int batch, double in
                       int8_t* qx_out, float* sx_out, int32_t* acc_gate, int32_t* acc_up,
                       float* salience, void* ws, size_t ws_bytes, void* stream);
 
-/* Test hook for the single-token path whose Stage-2 kernel selects its channels itself
- * (prox_ffn_forward with one token and no idx_out takes it): runs that path on x [1][d_model]
+/* Test hook for a single-token variant whose Stage-2 kernel selects its channels itself
+ * (the top-k folded into Stage 2's front; prox_ffn_forward keeps the separate top-k, which
+ * measured faster): runs that variant on x [1][d_model]
  * and also writes every selected channel to sel_out [k] int32 (device): first the channels
  * above the histogram bin of the k-th salience, in ascending order, then the winners inside
  * that bin, in ascending order. PROX_ERR_UNSUPPORTED if the shape or sparsity does not take
@@ -211,7 +216,8 @@ int prox_debug_fused_forward(const prox_packed* w, const float* x, double sparsi
                              double input_sparsity, float* y, int32_t* sel_out, void* ws,
                              size_t ws_bytes, void* stream);
 
-/* Test hook for the batch path: the ascending union of the rows of idx [batch][k]
+/* Test hook for the union kernel (the CUDA-core batch path of prox_sparse_ffn_noalloc):
+ * the ascending union of the rows of idx [batch][k]
  * (device int32) and, per union entry, a bit mask of the tokens that selected it.
  *   union_out [d_ff] int32, bits_out [d_ff] uint32, count_out [1] int32: device. */
 int prox_debug_union(const int32_t* idx, int batch, int k, int d_ff,
