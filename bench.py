@@ -61,6 +61,23 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(v: float, world: int, device: str) -> float:
+    """The maximum of v over all ranks (each rank's own v when running alone)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, seconds: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank units (weak scaling) and the
+    job took the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def workload_name(batch, sparsity, s_in):
     return (f"llama3-8b-ffn-4096x14336-b{batch}-s{round(sparsity * 100)}"
             f"-in{round(s_in * 100)}")
@@ -149,23 +166,34 @@ def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds):
 
 
 def run_reference(args):
+    """The reference arm: the fp64 CPU oracle on the host cores, same workload, metric and
+    unit as the GPU arm. A step is one token of the workload through the oracle's whole path
+    (about a second each), so the timed steps are bounded by time rather than by --steps."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    import numpy as np
+    import oracle as O
     import workloads as WL
     mats = WL.make_layer(WORKLOAD_KEY, 0)
-    X = WL.make_tokens(WORKLOAD_KEY, range(args.tokens))
+    X = WL.make_tokens(WORKLOAD_KEY, range(max(args.tokens, args.batch)))
+    d, F = mats["w_gate"].shape[1], mats["w_gate"].shape[0]
+    ol = O.prepare_layer(*(mats[n].float().numpy() for n in ("w_gate", "w_up", "w_down")))
+    warm = min(max(args.warmup, 0), 3)
+    for i in range(warm):
+        O.ffn_token(ol, np.asarray(X[i % len(X)]), args.sparsity, args.input_sparsity)
     budget = min(120.0, max(5.0, args.cpu_seconds * 4))
     rate, n, dt, threads = cpu_oracle_rate(mats, X, args.sparsity, args.input_sparsity, budget)
-    sample = (f"{n} tokens (batch 1) of the {workload_name(1, args.sparsity, args.input_sparsity)}"
-              f" workload through the fp64 numpy oracle in {dt:.1f} s; the run is bounded by "
-              f"time, not by --steps")
+    sample = (f"{n} tokens of the {workload_name(args.batch, args.sparsity, args.input_sparsity)}"
+              f" workload through the fp64 numpy oracle in {dt:.1f} s (tokens are independent, so "
+              f"the rate holds for any batch); bounded by time: {args.steps} steps were requested")
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": 0,
-            "steps": n, "warmup": 0, "ms_per_step": 1000.0 * dt / n, "higher_is_better": True,
+            "steps": n, "warmup": warm, "ms_per_step": 1000.0 * dt / n, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_name(args.batch, args.sparsity, args.input_sparsity),
-                       "d_model": 4096, "d_ff": 14336, "batch": 1,
-                       "sparsity": args.sparsity, "input_sparsity": args.input_sparsity},
+                       "d_model": d, "d_ff": F, "batch": args.batch, "sparsity": args.sparsity,
+                       "input_sparsity": args.input_sparsity,
+                       "k": O.k_for(args.sparsity, F), "k_in": O.k_for(args.input_sparsity, d)},
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -246,11 +274,7 @@ def run_ours(args):
             dist.barrier()
 
     def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, "cuda")
 
     B, sp, s_in, L = args.batch, args.sparsity, args.input_sparsity, args.layers
     d, F = 4096, 14336
@@ -399,7 +423,7 @@ def run_ours(args):
     s_fwd = t_fwd / K
     s_s2 = t_s2 / K2
     s_dense = t_dense / Kd
-    value = world * B * K / t_fwd
+    value = job_rate(world, B * K, t_fwd)
     achieved = s2_bytes / s_s2 / 1e9
     s2_kernel = "stage2_kernel" if B == 1 else "stage2_tc_kernel"
     traffic, traffic_note = profiled_traffic(s2_kernel)
@@ -438,7 +462,7 @@ def run_ours(args):
                      "us_per_launch": 1e6 * s_s2,
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "traffic_note": traffic_note},
-        "e2e": {"value": world * B * Ke / t_e2e, "unit": UNIT,
+        "e2e": {"value": job_rate(world, B * Ke, t_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": B * d * 4, "d2h_bytes_per_step": B * d * 4,
                 "api": "prox_ffn_forward_host (pinned host x/y, synchronous per step)"},
         "gpu_launches": K * per_step_kernels,
