@@ -144,24 +144,31 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds):
-    """Tokens/s of the CPU oracle's whole path on this host, over a bounded sample."""
+def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds, threads=None):
+    """Tokens/s of the CPU oracle's whole path on this host, over a bounded sample; with
+    threads=1 the numerical libraries are limited to one thread for the sample."""
+    import contextlib
     import numpy as np
     import oracle as O
     try:
-        from threadpoolctl import threadpool_info
-        blas_threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        from threadpoolctl import threadpool_info, threadpool_limits
+        limit = threadpool_limits(threads) if threads else contextlib.nullcontext()
     except Exception:
-        blas_threads = len(os.sched_getaffinity(0))
+        threadpool_info, limit = None, contextlib.nullcontext()
     ol = O.prepare_layer(*(layer_mats[n].float().numpy() for n in ("w_gate", "w_up", "w_down")))
     n = 0
-    t0 = time.perf_counter()
-    while True:
-        O.ffn_token(ol, np.asarray(X[n % len(X)]), sparsity, s_in)
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    dt = time.perf_counter() - t0
+    with limit:
+        if threadpool_info is not None:
+            blas_threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        else:
+            blas_threads = threads or len(os.sched_getaffinity(0))
+        t0 = time.perf_counter()
+        while True:
+            O.ffn_token(ol, np.asarray(X[n % len(X)]), sparsity, s_in)
+            n += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        dt = time.perf_counter() - t0
     return n / dt, n, dt, blas_threads
 
 
@@ -229,23 +236,37 @@ def profiled_traffic(kernel: str) -> tuple[float | None, str | None]:
     return rec.get("dram_bytes_per_launch"), rec.get("note")
 
 
-def timed_graph_replays(torch, stream, graphs, barrier, name):
+def timed_graph_replays(torch, stream, graphs, barrier, name, per_graph=None):
     """Seconds for replaying `graphs` on `stream`, by CUDA events on that stream. The replays
-    sit in an NVTX range called `name`, so a profiler can be limited to them."""
+    sit in an NVTX range called `name`, so a profiler can be limited to them. If per_graph is
+    a list, the seconds of each replay (events between replays) are appended to it."""
     barrier()
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
     torch.cuda.nvtx.range_push(name)
     with torch.cuda.stream(stream):   # replays go to the stream the events are on
-        start.record(stream)
-        for g in graphs:
+        events[0].record(stream)
+        for i, g in enumerate(graphs):
             g.replay()
-        end.record(stream)
+            events[i + 1].record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
     barrier()
-    return start.elapsed_time(end) / 1000.0
+    if per_graph is not None:
+        per_graph += [events[i].elapsed_time(events[i + 1]) / 1000.0 for i in range(len(graphs))]
+    return events[0].elapsed_time(events[-1]) / 1000.0
+
+
+def step_stats(chunk_seconds, chunk_steps):
+    """Median, 10th and 90th percentile of the microseconds per step over replayed chunks of
+    chunk_steps steps each (nearest-rank percentiles)."""
+    per = sorted(1e6 * t / n for t, n in zip(chunk_seconds, chunk_steps) if n > 0)
+    if not per:
+        return None
+
+    def pct(q):
+        return per[min(len(per) - 1, max(0, int(round(q * (len(per) - 1)))))]
+    return {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9), "chunks": len(per)}
 
 
 def capture(torch, stream, fn, n):
@@ -335,14 +356,19 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {P.prox_error_string(st)}")
 
+    graph_steps = {}   # steps per captured graph
+
     def graphs_for(fn, K):
         chunk = min(K, 4 * cycle) if K > 0 else 0
         gs = []
         if chunk:
             g = capture(torch, stream, fn, chunk)
+            graph_steps[id(g)] = chunk
             gs += [g] * (K // chunk)
             if K % chunk:
-                gs.append(capture(torch, stream, fn, K % chunk))
+                g2 = capture(torch, stream, fn, K % chunk)
+                graph_steps[id(g2)] = K % chunk
+                gs.append(g2)
         return gs
 
     K = args.steps
@@ -361,7 +387,13 @@ def run_ours(args):
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
-    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier, "timed_fwd"))
+    chunk_t = []
+    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier, "timed_fwd",
+                                               per_graph=chunk_t))
+    chunk_n = []
+    for g in g_fwd:
+        chunk_n.append(graph_steps[id(g)])
+    fwd_stats = step_stats(chunk_t, chunk_n)
     clocks = sampler.stop()
     del g_fwd
 
@@ -431,7 +463,11 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, n, dt, threads = cpu_oracle_rate(mats0, X_np, sp, s_in, args.cpu_seconds)
+        rate1, n1, dt1, _ = cpu_oracle_rate(mats0, X_np, sp, s_in, args.cpu_seconds, threads=1)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "value_1core": rate1,
+               "sample_1core": f"{n1} tokens in {dt1:.1f} s with the numerical libraries "
+                               f"limited to one thread",
                "sample": f"{n} tokens (batch 1) of this workload, layer 0, through the fp64 "
                          f"numpy oracle in {dt:.1f} s"}
 
@@ -449,6 +485,7 @@ def run_ours(args):
                          f"({L * layers[0].buffer.numel() / 1e9:.2f} GB)",
                    "parallelism": f"replicas x{world}"},
         "us_per_layer": 1e6 * s_fwd,
+        "us_per_layer_chunks": fwd_stats,
         "hbm_gbs_path": path_bytes / s_fwd / 1e9,
         "path_frac": path_bytes / s_fwd / 1e9 / hbm_peak,
         "algorithmic_bytes_per_step": path_bytes,
