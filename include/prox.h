@@ -46,7 +46,7 @@ extern "C" {
 #define PROX_ERR_CUDA        (-3)  /* a CUDA runtime call or launch failed                 */
 #define PROX_ERR_TIMEOUT     (-4)  /* device status: a bounded wait ran out                */
 #define PROX_ERR_BOUNDS      (-5)  /* device status: an index was out of range             */
-#define PROX_ERR_UNSUPPORTED (-6)  /* valid request this build does not implement          */
+#define PROX_ERR_UNSUPPORTED (-6)  /* valid request the library does not implement        */
 
 #define PROX_GROUP      128        /* proxy quantization group along d_model               */
 #define PROX_MAX_BATCH  16         /* tokens per call                                      */
