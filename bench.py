@@ -494,7 +494,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "kernel": (f"{s2_kernel} (+ its fixed-order partial-sum reduce"
-                                + (")" if B == 1 else " and the bf16 split of x)")),
+                                + (")" if B == 1 else
+                                   ", the batch's channel bitmap and the bf16 split of x)")),
                      "algorithmic_bytes_per_launch": s2_bytes,
                      "us_per_launch": 1e6 * s_s2,
                      "peak_source": f"{peak_src} HBM copy bandwidth",
