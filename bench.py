@@ -1,22 +1,29 @@
 """Benchmark of the Prox sparse SwiGLU FFN decode path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--batch B] [--sparsity S] [--input-sparsity S_in] [--layers L]
+                    [--workload 1..5] [--batch B] [--sparsity S] [--input-sparsity S_in]
+                    [--layers L]
 
-Workload: one Llama-3-8B-shaped FFN layer (d_model 4096, d_ff 14336), bf16 weights
-N(0, 0.02^2), inputs Student-t(4), 70% channel sparsity and 50% input sparsity, batch 1
-(seeded synthetic data, see workloads/). A step is one pass of the whole hot path (input
-selection, Stage-1 proxy GEMV + salience, top-k, Stage-2 gather GEMV + SwiGLU + down
-projection) over one batch of tokens on one layer. Steps rotate over L independently seeded
-layer copies (4 x 0.41 GB by default), so every step streams its weights from HBM rather
-than from the 126 MB L2. The K timed steps are replayed from CUDA graphs on one stream and
-timed with CUDA events; with torchrun each rank runs its own replica on its own GPU
-(independent tokens, no collective on the data path) and the slowest rank's time counts.
+Workloads (seeded synthetic data, see workloads/):
+  1  1024 x 2816 layer, N(0,1) inputs with 1% x20 outliers, 50% channel / 50% input sparsity
+  2  Llama-2-7B-shaped 4096 x 11008 layer, per-channel LogNormal weight scales, Student-t(4)
+  3  Llama-3-8B-shaped 4096 x 14336 layer, Student-t(4), 70% / 50% (the default)
+  4  decode step through 32 independently seeded 4096 x 14336 layers with a unit-gain RMSNorm
+     between them (one step = one token through all 32 layers)
+  5  Llama-2-70B-shaped 8192 x 28672 layer, per-channel LogNormal scales, Student-t(3)
+A step is one pass of the whole hot path (input selection, Stage-1 proxy GEMV + salience,
+top-k, Stage-2 gather GEMV + SwiGLU + down projection) over one batch of tokens on one layer
+(on all 32 layers for workload 4). Steps rotate over independently seeded layer copies whose
+total size is several times the 126 MB L2, so every step streams its weights from HBM. The K
+timed steps are replayed from CUDA graphs on one stream and timed with CUDA events on that
+stream; with torchrun each rank runs its own replica on its own GPU (independent tokens, no
+collective on the data path) and the slowest rank's time counts.
 
-One JSON line is printed (rank 0): the metric (tokens/s per layer), the Stage-2 kernel's
-roofline fraction against the measured HBM copy bandwidth, the dense-FFN speedup, the
-end-to-end number through the host-buffer entry point, SM clocks sampled during the timed
-region, and the CPU oracle timed on a bounded sample on the host cores.
+One JSON line is printed (rank 0): the metric (tokens/s per layer) over exactly the K timed
+steps, the per-chunk spread of a longer run of the same graph, the Stage-2 kernel's roofline
+fraction against the measured HBM copy bandwidth, the dense-FFN speedup, the end-to-end
+number through the host-buffer entry point, SM clocks sampled during the timed region, and
+the CPU oracle timed on a bounded sample on the host cores.
 """
 from __future__ import annotations
 
@@ -35,23 +42,30 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse SwiGLU FFN decode tokens/s/layer"
 UNIT = "tokens/s/layer"
-WORKLOAD_KEY = 3   # the Llama-3-8B-shaped 4096 x 14336 layer of the workloads module
+DEFAULT_WORKLOAD = 3   # the Llama-3-8B-shaped 4096 x 14336 layer
+L2_BYTES = 126 * 2 ** 20
+CHAIN_WORKLOAD = 4     # the 32-layer stack
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 20000; 400 for the 32-layer stack)")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--batch", type=int, default=1)
-    ap.add_argument("--sparsity", type=float, default=0.7)
-    ap.add_argument("--input-sparsity", type=float, default=0.5)
-    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--workload", type=int, choices=[1, 2, 3, 4, 5], default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--sparsity", type=float, default=None)
+    ap.add_argument("--input-sparsity", type=float, default=None)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layer copies the steps rotate over (default: enough for 3x L2)")
     ap.add_argument("--tokens", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--spread-ms", type=float, default=300.0,
+                    help="wall time of the extra chunked run that gives the p10/p50/p90 spread")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -78,13 +92,50 @@ def job_rate(world: int, units_per_rank: float, seconds: float) -> float:
     return world * units_per_rank / seconds
 
 
-def workload_name(batch, sparsity, s_in):
-    return (f"llama3-8b-ffn-4096x14336-b{batch}-s{round(sparsity * 100)}"
-            f"-in{round(s_in * 100)}")
+# ----------------------------------------------------------------------------- workload
+
+def resolve(args) -> dict:
+    """The workload's shape and the run's batch, sparsities, layer copies and chain depth."""
+    import workloads as WL
+    w = WL.WORKLOADS[args.workload]
+    batch = args.batch if args.batch is not None else w.batches[0]
+    sp = args.sparsity if args.sparsity is not None else (0.7 if 0.7 in w.sparsities
+                                                          else w.sparsities[0])
+    s_in = args.input_sparsity if args.input_sparsity is not None else w.input_sparsity
+    chain = args.workload == CHAIN_WORKLOAD
+    d, F = w.d_model, w.d_ff
+    packed = d * F + 4 * (d // 128) * F + 6 * F * d
+    if chain:
+        layers = w.layers
+    elif args.layers is not None:
+        layers = args.layers
+    else:
+        layers = max(4, math.ceil(3 * L2_BYTES / packed))
+    name = (f"{w.name}-b{batch}-s{round(sp * 100)}-in{round(s_in * 100)}")
+    return {"key": args.workload, "name": name, "d": d, "F": F, "batch": batch,
+            "sparsity": sp, "input_sparsity": s_in, "layers": layers, "chain": chain,
+            "depth": w.layers if chain else 1, "packed_bytes": packed}
+
+
+def workload_config(cfg: dict, world: int, tokens: int, k: int, k_in: int) -> dict:
+    """The `config` object of the JSON line (identical for both arms; k and k_in come from
+    the arm's own implementation of the kept-count rule)."""
+    c = {"workload": cfg["name"], "d_model": cfg["d"], "d_ff": cfg["F"],
+         "batch": cfg["batch"], "sparsity": cfg["sparsity"],
+         "input_sparsity": cfg["input_sparsity"], "k": k, "k_in": k_in,
+         "layer_copies": cfg["layers"], "tokens": tokens,
+         "l2": (f"inputs larger than L2: steps rotate over {cfg['layers']} layer copies "
+                f"({cfg['layers'] * cfg['packed_bytes'] / 1e9:.2f} GB)"),
+         "parallelism": f"replicas x{world}"}
+    if cfg["chain"]:
+        c["layers_per_step"] = cfg["depth"]
+        c["l2"] = (f"inputs larger than L2: each step runs through {cfg['depth']} layers "
+                   f"({cfg['depth'] * cfg['packed_bytes'] / 1e9:.2f} GB)")
+    return c
 
 
 def algorithmic_bytes(d, F, k_in_rows, k_rows, batch):
-    """Bytes the method must move per step: kept int4 proxy rows (gate+up, one byte per
+    """Bytes the method must move per layer pass: kept int4 proxy rows (gate+up, one byte per
     channel), fp16 group scales of both proxies, the selected bf16 rows of W_gate, W_up and
     W_down^T, plus x, y, the mask and the salience."""
     G = d // 128
@@ -106,7 +157,6 @@ class ClockSampler:
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
-        self.lines: list[str] = []
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -128,25 +178,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [ln.split(",") for ln in out.strip().splitlines() if ln.count(",") >= 7]
-        if not rows:
-            return None
-        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
-        smax = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4)
-                          if r[4 + i].strip().lower() == "active"})
-        under_load = [v for v in sm if smax and v >= 0.5 * max(smax)] or sm
-        return {"sm_mhz": statistics.median(under_load) if under_load else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows)}
+        return summarize_clocks(out)
+
+
+def summarize_clocks(text: str) -> dict | None:
+    rows = [ln.split(",") for ln in text.strip().splitlines() if ln.count(",") >= 7]
+    if not rows:
+        return None
+    sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+    smax = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4)
+                      if r[4 + i].strip().lower() == "active"})
+    under_load = [v for v in sm if smax and v >= 0.5 * max(smax)] or sm
+    return {"sm_mhz": statistics.median(under_load) if under_load else None,
+            "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+            "samples": len(rows)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds, threads=None):
-    """Tokens/s of the CPU oracle's whole path on this host, over a bounded sample; with
-    threads=1 the numerical libraries are limited to one thread for the sample."""
+def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds, threads=None, max_tokens=None):
+    """Tokens/s of the CPU oracle's whole path on this host, over a bounded sample (at least
+    one token, then until `seconds` have passed or max_tokens are done); with threads=1 the
+    numerical libraries are limited to one thread for the sample."""
     import contextlib
     import numpy as np
     import oracle as O
@@ -166,41 +221,80 @@ def cpu_oracle_rate(layer_mats, X, sparsity, s_in, seconds, threads=None):
         while True:
             O.ffn_token(ol, np.asarray(X[n % len(X)]), sparsity, s_in)
             n += 1
-            if time.perf_counter() - t0 >= seconds:
+            if time.perf_counter() - t0 >= seconds or (max_tokens and n >= max_tokens):
                 break
         dt = time.perf_counter() - t0
     return n / dt, n, dt, blas_threads
 
 
 def run_reference(args):
-    """The reference arm: the fp64 CPU oracle on the host cores, same workload, metric and
-    unit as the GPU arm. A step is one token of the workload through the oracle's whole path
-    (about a second each), so the timed steps are bounded by time rather than by --steps."""
+    """The reference arm: the fp64 CPU oracle on the host cores, on the GPU arm's workload,
+    config, metric and unit. A step is one batch of the workload's tokens through the oracle's
+    whole path (for the 32-layer stack: one token through every layer, RMSNorm between); W
+    untimed steps, then exactly K timed steps, unless K steps would run past a ten-minute
+    budget, in which case the steps that fit are timed and the line says so."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import numpy as np
     import oracle as O
     import workloads as WL
-    mats = WL.make_layer(WORKLOAD_KEY, 0)
-    X = WL.make_tokens(WORKLOAD_KEY, range(max(args.tokens, args.batch)))
-    d, F = mats["w_gate"].shape[1], mats["w_gate"].shape[0]
-    ol = O.prepare_layer(*(mats[n].float().numpy() for n in ("w_gate", "w_up", "w_down")))
-    warm = min(max(args.warmup, 0), 3)
+    cfg = resolve(args)
+    B = cfg["batch"]
+    depth = cfg["depth"]
+    n_layers = depth if cfg["chain"] else 1
+    ols = []
+    for li in range(n_layers):
+        m = WL.make_layer(cfg["key"], li)
+        ols.append(O.prepare_layer(*(m[n].float().numpy() for n in ("w_gate", "w_up", "w_down"))))
+    T = max(B, args.tokens // B * B)
+    X = WL.make_tokens(cfg["key"], range(T))
+    nb = T // B
+
+    def step(i):
+        xs = X[(i % nb) * B:(i % nb + 1) * B]
+        for x in xs:
+            xc = np.asarray(x, np.float64)
+            for li, ol in enumerate(ols):
+                out = O.ffn_token(ol, xc.astype(np.float32), cfg["sparsity"],
+                                  cfg["input_sparsity"])
+                xc = O.rmsnorm(out["y"][None])[0] if li + 1 < len(ols) else out["y"]
+
+    warm = max(0, args.warmup if args.warmup is not None else 3)
+    warm = min(warm, 3)
     for i in range(warm):
-        O.ffn_token(ol, np.asarray(X[i % len(X)]), args.sparsity, args.input_sparsity)
-    budget = min(120.0, max(5.0, args.cpu_seconds * 4))
-    rate, n, dt, threads = cpu_oracle_rate(mats, X, args.sparsity, args.input_sparsity, budget)
-    sample = (f"{n} tokens of the {workload_name(args.batch, args.sparsity, args.input_sparsity)}"
-              f" workload through the fp64 numpy oracle in {dt:.1f} s (tokens are independent, so "
-              f"the rate holds for any batch); bounded by time: {args.steps} steps were requested")
+        step(i)
+    budget = 600.0
+    t0 = time.perf_counter()
+    n = 0
+    per_step = None
+    while n < args.steps:
+        step(warm + n)
+        n += 1
+        el = time.perf_counter() - t0
+        per_step = el / n
+        if el + per_step > budget:
+            break
+    dt = time.perf_counter() - t0
+    threads = len(os.sched_getaffinity(0))
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [threads])
+    except Exception:
+        pass
+    units = n * B * (depth if cfg["chain"] else 1)
+    rate = units / dt
+    sample = (f"{n} steps of batch {B} ({n * B} tokens"
+              + (f" x {depth} layers" if cfg["chain"] else "")
+              + f") of the {cfg['name']} workload through the fp64 numpy oracle in {dt:.1f} s")
+    if n < args.steps:
+        sample += f"; {args.steps} steps were requested, stopped at the {budget:.0f} s budget"
     line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": 0,
-            "steps": n, "warmup": warm, "ms_per_step": 1000.0 * dt / n, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_name(args.batch, args.sparsity, args.input_sparsity),
-                       "d_model": d, "d_ff": F, "batch": args.batch, "sparsity": args.sparsity,
-                       "input_sparsity": args.input_sparsity,
-                       "k": O.k_for(args.sparsity, F), "k_in": O.k_for(args.input_sparsity, d)},
+            "steps": n, "warmup": warm, "ms_per_step": 1000.0 * dt / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": workload_config(cfg, world, T, O.k_for(cfg["sparsity"], cfg["F"]),
+                                      O.k_for(cfg["input_sparsity"], cfg["d"])),
             "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -221,14 +315,14 @@ def source_hash(names=None) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str) -> tuple[float | None, str | None]:
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current sources of that kernel (its translation unit and the headers it includes,
-    listed in the record)."""
+def profiled_traffic(kernel: str, workload: str) -> tuple[float | None, str | None]:
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, if it was
+    taken on the current sources of that kernel (its translation unit and the headers it
+    includes, listed in the record)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f).get(kernel)
+            rec = json.load(f).get(f"{kernel}@{workload}")
     except (OSError, ValueError):
         return None, None
     if not rec or rec.get("source_hash") != source_hash(rec.get("sources")):
@@ -269,12 +363,24 @@ def step_stats(chunk_seconds, chunk_steps):
     return {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9), "chunks": len(per)}
 
 
-def capture(torch, stream, fn, n):
+def capture(torch, stream, fn, n, start=0):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        for i in range(n):
+        for i in range(start, start + n):
             fn(i)
     return g
+
+
+def plan_chunks(K: int, cycle: int) -> list[int]:
+    """Step counts of the graphs that together replay exactly K steps: chunks of a whole
+    number of rotation cycles (at most 4), then the remainder."""
+    if K <= 0:
+        return []
+    chunk = max(1, min(K, 4 * cycle))
+    out = [chunk] * (K // chunk)
+    if K % chunk:
+        out.append(K % chunk)
+    return out
 
 
 def run_ours(args):
@@ -297,57 +403,92 @@ def run_ours(args):
     def max_over_ranks(v: float) -> float:
         return reduce_max(v, world, "cuda")
 
-    B, sp, s_in, L = args.batch, args.sparsity, args.input_sparsity, args.layers
-    d, F = 4096, 14336
+    cfg = resolve(args)
+    B, sp, s_in, L = cfg["batch"], cfg["sparsity"], cfg["input_sparsity"], cfg["layers"]
+    d, F, chain, depth = cfg["d"], cfg["F"], cfg["chain"], cfg["depth"]
     k, k_in = P.prox_k_for(sp, F), P.prox_k_for(s_in, d)
     T = max(B, args.tokens // B * B)
 
     layers, mats0 = [], None
     for li in range(L):
-        mats = WL.make_layer(WORKLOAD_KEY, li)
+        mats = WL.make_layer(cfg["key"], li)
         if li == 0:
             mats0 = mats
         dev = {n: v.cuda() for n, v in mats.items() if n.startswith("w_")}
         layers.append(P.prox_pack_weights(dev["w_gate"], dev["w_up"], dev["w_down"]))
         del dev
     torch.cuda.synchronize()
-    X_np = WL.make_tokens(WORKLOAD_KEY, range(rank * T, (rank + 1) * T))
+    X_np = WL.make_tokens(cfg["key"], range(rank * T, (rank + 1) * T))
     X = torch.from_numpy(X_np).cuda()
     Y = torch.empty_like(X)
+    Xa = torch.empty((2, B, d), dtype=torch.float32, device="cuda")   # chain activations
+    Ya = torch.empty((B, d), dtype=torch.float32, device="cuda")
     ws = P.prox_workspace(d, F, B)
     stream = torch.cuda.Stream()
     nb_batches = T // B
-    # one token: input_quant, Stage 1, top-k, Stage 2, reduce; a batch adds split_x (the
-    # tensor-core Stage 2 takes its activations as bf16 pairs)
-    per_step_kernels = 5 if B == 1 else 6
+
+    def layer_of(i):
+        return i % L
+
+    def batch_of(i):
+        return (i // L) % nb_batches if not chain else i % nb_batches
 
     def step_fwd(i):
-        li, t = i % L, (i // L) % nb_batches
-        P.prox_ffn_forward(layers[li], X[t * B:(t + 1) * B], sp, s_in, ws,
-                           y=Y[t * B:(t + 1) * B], stream=stream)
+        t = batch_of(i)
+        if chain:
+            xin = X[t * B:(t + 1) * B]
+            for li in range(depth):
+                out = Y[t * B:(t + 1) * B] if li + 1 == depth else Ya
+                P.prox_ffn_forward(layers[li], xin, sp, s_in, ws, y=out, stream=stream)
+                if li + 1 < depth:
+                    P.prox_rmsnorm(Ya, 1e-6, out=Xa[li % 2], stream=stream)
+                    xin = Xa[li % 2]
+        else:
+            P.prox_ffn_forward(layers[layer_of(i)], X[t * B:(t + 1) * B], sp, s_in, ws,
+                               y=Y[t * B:(t + 1) * B], stream=stream)
 
     def step_dense(i):
-        li, t = i % L, (i // L) % nb_batches
-        P.prox_dense_ffn(layers[li], X[t * B:(t + 1) * B], ws, y=Y[t * B:(t + 1) * B],
-                         stream=stream)
+        t = batch_of(i)
+        if chain:
+            xin = X[t * B:(t + 1) * B]
+            for li in range(depth):
+                out = Y[t * B:(t + 1) * B] if li + 1 == depth else Ya
+                P.prox_dense_ffn(layers[li], xin, ws, y=out, stream=stream)
+                if li + 1 < depth:
+                    P.prox_rmsnorm(Ya, 1e-6, out=Xa[li % 2], stream=stream)
+                    xin = Xa[li % 2]
+        else:
+            P.prox_dense_ffn(layers[layer_of(i)], X[t * B:(t + 1) * B], ws,
+                             y=Y[t * B:(t + 1) * B], stream=stream)
 
-    # masks of every (layer, token batch) pair, for timing Stage 2 alone
-    cycle = L * nb_batches
-    masks = []
+    # the (layer, input, mask) triples of one rotation cycle, for timing Stage 2 alone; in the
+    # chain each layer's input is the previous layer's normalised output
+    cycle = nb_batches if chain else L * nb_batches
+    s2_items = []
     with torch.cuda.stream(stream):
         for i in range(cycle):
-            li, t = i % L, (i // L) % nb_batches
-            masks.append(P.prox_build_mask(layers[li], X[t * B:(t + 1) * B], sp, s_in, ws,
-                                           stream=stream))
+            t = batch_of(i)
+            if chain:
+                xin = X[t * B:(t + 1) * B].clone()
+                for li in range(depth):
+                    idx = P.prox_build_mask(layers[li], xin, sp, s_in, ws, stream=stream)
+                    s2_items.append((li, xin, idx))
+                    y = P.prox_ffn_forward(layers[li], xin, sp, s_in, ws, stream=stream)
+                    xin = P.prox_rmsnorm(y, 1e-6, stream=stream)
+            else:
+                xin = X[t * B:(t + 1) * B]
+                idx = P.prox_build_mask(layers[layer_of(i)], xin, sp, s_in, ws, stream=stream)
+                s2_items.append((layer_of(i), xin, idx))
+    torch.cuda.synchronize()
+    n_s2 = len(s2_items)
 
     def step_s2(i):
-        li, t = i % L, (i // L) % nb_batches
-        P.prox_sparse_ffn(layers[li], X[t * B:(t + 1) * B], masks[i % cycle], ws,
-                          y=Y[t * B:(t + 1) * B], stream=stream)
+        li, xin, idx = s2_items[i % n_s2]
+        P.prox_sparse_ffn(layers[li], xin, idx, ws, y=Ya, stream=stream)
 
-    # warm-up (also sets kernel attributes before any capture)
+    warm = max(3, args.warmup)
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
+        for i in range(warm):
             step_fwd(i)
             step_dense(i)
             step_s2(i)
@@ -356,26 +497,32 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {P.prox_error_string(st)}")
 
-    graph_steps = {}   # steps per captured graph
-
-    def graphs_for(fn, K):
-        chunk = min(K, 4 * cycle) if K > 0 else 0
+    def graphs_for(fn, K, cyc):
+        """Graphs replaying exactly K steps of fn, and the steps each one holds; every
+        distinct graph is replayed once, untimed, before it is timed (graph upload)."""
+        plan = plan_chunks(K, cyc)
+        built = {}
         gs = []
-        if chunk:
-            g = capture(torch, stream, fn, chunk)
-            graph_steps[id(g)] = chunk
-            gs += [g] * (K // chunk)
-            if K % chunk:
-                g2 = capture(torch, stream, fn, K % chunk)
-                graph_steps[id(g2)] = K % chunk
-                gs.append(g2)
-        return gs
+        for n in plan:
+            if n not in built:
+                built[n] = capture(torch, stream, fn, n)
+                with torch.cuda.stream(stream):
+                    built[n].replay()
+            gs.append(built[n])
+        torch.cuda.synchronize()
+        return gs, plan
+
+    # launches per step, counted by the library while one step is recorded
+    c0 = P.prox_launch_count()
+    g_probe = capture(torch, stream, step_fwd, 1)
+    launches_per_step = P.prox_launch_count() - c0
+    del g_probe
 
     K = args.steps
-    g_fwd = graphs_for(step_fwd, K)
-    with torch.cuda.stream(stream):
-        if g_fwd:
-            g_fwd[0].replay()
+    g_fwd, plan_fwd = graphs_for(step_fwd, K, cycle)
+    with torch.cuda.stream(stream):   # bring the clocks up before the timed region
+        for g in g_fwd[:2]:
+            g.replay()
     torch.cuda.synchronize()
 
     uuid = None
@@ -387,38 +534,60 @@ def run_ours(args):
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
+    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier, "timed_fwd"))
+    # the spread: the same path replayed in chunks of about 1/20 of spread_ms each, for at
+    # least spread_ms in total (outside the K-step measurement above)
+    est = t_fwd / max(K, 1)
+    per_chunk = max(1, int(args.spread_ms / 1000.0 / 20 / max(est, 1e-9)))
+    per_chunk = min(per_chunk, 4 * cycle)
+    g_sp = capture(torch, stream, step_fwd, per_chunk)
+    with torch.cuda.stream(stream):
+        g_sp.replay()
     chunk_t = []
-    t_fwd = max_over_ranks(timed_graph_replays(torch, stream, g_fwd, barrier, "timed_fwd",
-                                               per_graph=chunk_t))
-    chunk_n = []
-    for g in g_fwd:
-        chunk_n.append(graph_steps[id(g)])
-    fwd_stats = step_stats(chunk_t, chunk_n)
+    timed_graph_replays(torch, stream, [g_sp] * 20, barrier, "spread_fwd", per_graph=chunk_t)
+    fwd_stats = step_stats(chunk_t, [per_chunk] * len(chunk_t))
     clocks = sampler.stop()
-    del g_fwd
+    del g_fwd, g_sp
 
-    K2 = min(K, 20000)
-    g_s2 = graphs_for(step_s2, K2)
+    K2 = min(K * depth, 20000)
+    g_s2, _ = graphs_for(step_s2, K2, n_s2)
     t_s2 = max_over_ranks(timed_graph_replays(torch, stream, g_s2, barrier, "timed_stage2"))
     del g_s2
-    Kd = min(K, 5000)
-    g_d = graphs_for(step_dense, Kd)
+    Kd = max(1, min(K, 5000 // depth))
+    g_d, _ = graphs_for(step_dense, Kd, cycle)
     t_dense = max_over_ranks(timed_graph_replays(torch, stream, g_d, barrier, "timed_dense"))
     del g_d
 
-    # end to end through the host-buffer entry point: H2D of x, the path, D2H of y, each step
-    Ke = min(K, 3000)
+    # end to end through the public API with host buffers: H2D of x, the path (all layers for
+    # the stack), D2H of y, every step
+    Ke = max(1, min(K, 3000 // depth))
     xh = torch.from_numpy(X_np).pin_memory()
     yh = torch.empty((B, d), dtype=torch.float32).pin_memory()
+
+    def e2e_step(i):
+        t = batch_of(i)
+        if not chain:
+            P.prox_ffn_forward_host(layers[layer_of(i)], xh[t * B:(t + 1) * B], sp, s_in, ws,
+                                    y_host=yh, stream=stream)
+            return
+        with torch.cuda.stream(stream):
+            xin = Xa[0]
+            xin.copy_(xh[t * B:(t + 1) * B], non_blocking=True)
+            for li in range(depth):
+                P.prox_ffn_forward(layers[li], xin, sp, s_in, ws, y=Ya, stream=stream)
+                if li + 1 < depth:
+                    P.prox_rmsnorm(Ya, 1e-6, out=Xa[(li + 1) % 2], stream=stream)
+                    xin = Xa[(li + 1) % 2]
+            yh.copy_(Ya, non_blocking=True)
+        stream.synchronize()
+
     for i in range(3):
-        P.prox_ffn_forward_host(layers[i % L], xh[:B], sp, s_in, ws, y_host=yh, stream=stream)
+        e2e_step(i)
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(Ke):
-        li, t = i % L, (i // L) % nb_batches
-        P.prox_ffn_forward_host(layers[li], xh[t * B:(t + 1) * B], sp, s_in, ws, y_host=yh,
-                                stream=stream)
+        e2e_step(i)
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0)
     barrier()
@@ -430,17 +599,15 @@ def run_ours(args):
     if B == 1:
         rows_in, rows_ch = k_in, k
     else:
-        kept_sizes, union_sizes = [], []
+        kept_sizes = []
         for t in range(nb_batches):
-            xb = X_np[t * B:(t + 1) * B]
             kept = set()
-            for r in xb:
+            for r in X_np[t * B:(t + 1) * B]:
                 kept |= set(np.argsort(-np.abs(r), kind="stable")[:k_in].tolist())
             kept_sizes.append(len(kept))
-        for m in masks:
-            union_sizes.append(len(np.unique(m.cpu().numpy())))
+        union_sizes = [len(np.unique(it[2].cpu().numpy())) for it in s2_items]
         rows_in, rows_ch = statistics.mean(kept_sizes), statistics.mean(union_sizes)
-    path_bytes = algorithmic_bytes(d, F, rows_in, rows_ch, B)
+    path_bytes = algorithmic_bytes(d, F, rows_in, rows_ch, B) * depth
     s2_bytes = stage2_bytes(d, rows_ch, B)
 
     peaks = {}
@@ -455,10 +622,10 @@ def run_ours(args):
     s_fwd = t_fwd / K
     s_s2 = t_s2 / K2
     s_dense = t_dense / Kd
-    value = job_rate(world, B * K, t_fwd)
+    value = job_rate(world, B * K * depth, t_fwd)
     achieved = s2_bytes / s_s2 / 1e9
     s2_kernel = "stage2_kernel" if B == 1 else "stage2_tc_kernel"
-    traffic, traffic_note = profiled_traffic(s2_kernel)
+    traffic, traffic_note = profiled_traffic(s2_kernel, cfg["name"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -469,27 +636,25 @@ def run_ours(args):
                "sample_1core": f"{n1} tokens in {dt1:.1f} s with the numerical libraries "
                                f"limited to one thread",
                "sample": f"{n} tokens (batch 1) of this workload, layer 0, through the fp64 "
-                         f"numpy oracle in {dt:.1f} s"}
+                         f"numpy oracle in {dt:.1f} s (a token through one layer is the unit)"}
 
     if rank != 0:
         return
+    us_layer = 1e6 * s_fwd / depth
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": 1000.0 * s_fwd,
+        "warmup": warm, "ms_per_step": 1000.0 * s_fwd,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(B, sp, s_in), "d_model": d, "d_ff": F,
-                   "batch": B, "sparsity": sp, "input_sparsity": s_in, "k": k, "k_in": k_in,
-                   "layer_copies": L, "tokens": T,
-                   "l2": f"inputs larger than L2: steps rotate over {L} layer copies "
-                         f"({L * layers[0].buffer.numel() / 1e9:.2f} GB)",
-                   "parallelism": f"replicas x{world}"},
-        "us_per_layer": 1e6 * s_fwd,
-        "us_per_layer_chunks": fwd_stats,
+        "config": workload_config(cfg, world, T, k, k_in),
+        "us_per_layer": us_layer,
+        "us_per_step_chunks": fwd_stats,
+        "spread_note": (f"20 chunks of {per_chunk} steps replayed after the {K} timed steps; "
+                        "median/p10/p90 of the per-step time per chunk"),
         "hbm_gbs_path": path_bytes / s_fwd / 1e9,
         "path_frac": path_bytes / s_fwd / 1e9 / hbm_peak,
         "algorithmic_bytes_per_step": path_bytes,
-        "dense_us_per_layer": 1e6 * s_dense,
+        "dense_us_per_layer": 1e6 * s_dense / depth,
         "speedup_vs_dense": s_dense / s_fwd,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
@@ -500,10 +665,14 @@ def run_ours(args):
                      "us_per_launch": 1e6 * s_s2,
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "traffic_note": traffic_note},
-        "e2e": {"value": job_rate(world, B * Ke, t_e2e), "unit": UNIT,
+        "e2e": {"value": job_rate(world, B * Ke * depth, t_e2e), "unit": UNIT,
                 "h2d_bytes_per_step": B * d * 4, "d2h_bytes_per_step": B * d * 4,
-                "api": "prox_ffn_forward_host (pinned host x/y, synchronous per step)"},
-        "gpu_launches": K * per_step_kernels,
+                "api": ("prox_ffn_forward_host (pinned host x/y, synchronous per step)"
+                        if not chain else
+                        "pinned host x -> prox_ffn_forward + prox_rmsnorm through all layers "
+                        "-> pinned host y, synchronous per step")},
+        "gpu_launches": K * launches_per_step,
+        "launches_per_step": launches_per_step,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "dtype_detail": ("Stage 1: int4 x int8 products, exact int32 sums, fp32 double-float "
@@ -521,6 +690,8 @@ def run_ours(args):
 
 def main():
     args = parse()
+    if args.steps is None:
+        args.steps = 400 if args.workload == CHAIN_WORKLOAD else 20000
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -51,6 +51,7 @@ SIGNATURES = {
     "prox_get_status": (_i, [_vp, _vp]),
     "prox_error_string": (ctypes.c_char_p, [_i]),
     "prox_last_cuda_error": (ctypes.c_char_p, []),
+    "prox_launch_count": (ctypes.c_uint64, []),
     "prox_debug_stage1": (_i, [_P, _vp, _i, _d, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_union": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_fused_forward": (_i, [_P, _vp, _d, _d, _vp, _vp, _vp, _sz, _vp]),

@@ -242,6 +242,11 @@ def prox_get_status(ws: Workspace, stream=None) -> int:
     return int(_lib.lib().prox_get_status(ws.ptr, _stream(stream, ws.buffer.device)))
 
 
+def prox_launch_count() -> int:
+    """Kernel launches the library has enqueued in this process (graph captures count once)."""
+    return int(_lib.lib().prox_launch_count())
+
+
 def prox_error_string(code: int) -> str:
     return _lib.error_string(code)
 
@@ -309,6 +314,7 @@ __all__ = [
     "GROUP", "MAX_BATCH", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
     "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",
+    "prox_launch_count",
     "prox_k_for", "prox_pack_weights", "prox_packed_bytes", "prox_rmsnorm", "prox_sparse_ffn",
     "prox_sparse_ffn_noalloc",
     "prox_workspace", "prox_workspace_bytes", "prox_workspace_init",

@@ -351,6 +351,8 @@ int prox_get_status(void* ws, void* stream) {
 
 const char* prox_last_cuda_error(void) { return last_cuda_error(); }
 
+uint64_t prox_launch_count(void) { return launch_count(); }
+
 const char* prox_error_string(int code) {
     switch (code) {
         case PROX_OK: return "ok";

@@ -146,6 +146,11 @@ inline int cuda_ok(cudaError_t err, const char* what) {
     return err == cudaSuccess ? PROX_OK : cuda_fail(err, what);
 }
 
+// Counts one kernel launch enqueued by the library (for prox_launch_count). Every launch
+// site calls it once per launch it issues, including launches recorded into a CUDA graph.
+void count_launch();
+uint64_t launch_count();
+
 // Raises `fn`'s dynamic shared-memory limit on the current device to at least `bytes`. The
 // limit is a per-function, per-device setting that the runtime checks against static plus
 // dynamic shared memory, so every launch with dynamic shared memory goes through here; the
@@ -169,7 +174,9 @@ inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-    return err == cudaSuccess ? PROX_OK : cuda_fail(err, "kernel launch");
+    if (err != cudaSuccess) return cuda_fail(err, "kernel launch");
+    count_launch();
+    return PROX_OK;
 }
 
 int launch_pack(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down, int d,

@@ -1,5 +1,6 @@
 // Small kernels around the path: the unit-gain RMSNorm between stacked layers, an index
 // fill for the all-channels mask, and the bounded-wait probe used to test timeouts.
+#include <atomic>
 #include <cstdio>
 #include <map>
 #include <mutex>
@@ -20,6 +21,13 @@ int cuda_fail(cudaError_t err, const char* what) {
 }
 
 const char* last_cuda_error() { return g_last_cuda_error; }
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int ensure_dynamic_smem(const void* fn, size_t bytes) {
     static std::mutex mu;
@@ -80,18 +88,24 @@ __global__ void wait_probe_kernel(int* __restrict__ status, long long spin_cycle
 
 int launch_rmsnorm(const float* y, float* x_out, int batch, int d, float eps, cudaStream_t s) {
     rmsnorm_kernel<<<batch, 256, 0, s>>>(y, x_out, d, eps);
-    return cuda_ok(cudaGetLastError(), "rmsnorm launch");
+    const int rc = cuda_ok(cudaGetLastError(), "rmsnorm launch");
+    if (rc == PROX_OK) count_launch();
+    return rc;
 }
 
 int launch_iota(int32_t* out, int n, int rows, cudaStream_t s) {
     const int total = n * rows;
     iota_kernel<<<(total + 255) / 256, 256, 0, s>>>(out, n, rows);
-    return cuda_ok(cudaGetLastError(), "index fill launch");
+    const int rc = cuda_ok(cudaGetLastError(), "index fill launch");
+    if (rc == PROX_OK) count_launch();
+    return rc;
 }
 
 int launch_wait_probe(int* status, long long spin_cycles, cudaStream_t s) {
     wait_probe_kernel<<<1, 32, 0, s>>>(status, spin_cycles);
-    return cuda_ok(cudaGetLastError(), "wait probe launch");
+    const int rc = cuda_ok(cudaGetLastError(), "wait probe launch");
+    if (rc == PROX_OK) count_launch();
+    return rc;
 }
 
 }  // namespace prox

@@ -539,7 +539,9 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
         static_cast<const float*>(reinterpret_cast<const float*>(ws + W.sx)), pl.gps, pl.S, B,
         sigma, reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up,
         &reinterpret_cast<Control*>(ws + W.control)->status);
-    return err == cudaSuccess ? PROX_OK : cuda_fail(err, "Stage-1 cluster launch");
+    if (err != cudaSuccess) return cuda_fail(err, "Stage-1 cluster launch");
+    count_launch();
+    return PROX_OK;
 }
 
 int launch_stage1(const uint8_t* packed, const PackedLayout& L, int d, int F, int B, uint8_t* ws,

@@ -127,7 +127,10 @@ int prox_build_mask(const prox_packed* w, const float* x, int batch,
 int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx,
                     int k, float* y, void* ws, size_t ws_bytes, void* stream);
 
-/* The whole path: Stage 1 mask, then Stage 2 over it. At sparsity 0 every channel is kept
+/* The whole path: Stage 1 mask, then Stage 2 over it (technical summary, "Methodology: The
+ * Prox Framework": Stage 1 "Lightweight Proxy Construction" builds the shared mask m_s, Stage
+ * 2 "Exact Sparse Computation" computes the masked channels exactly; the authors' abstract:
+ * all three projections run sparse under the one mask). At sparsity 0 every channel is kept
  * and Stage 1 is skipped (the result is the dense FFN).
  *   y       [batch][d_model] fp32 device (written).
  *   idx_out [batch][k] int32 device, or NULL when the mask is not wanted. */
@@ -157,7 +160,9 @@ int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch,
  *   by every GPU that loads the library until the process exits. A call needs
  *   256 + 8*d_ff + SMs * tile * d_model * 4 bytes (rounded to 256-byte pieces), where tile
  *   is the batch's token tile (1 for one token, 2 for two, up to 4 when d_model <= 4096);
- *   with 148 SMs that allows one token up to d_model 8192. Larger requests return
+ *   with 148 SMs and d_ff up to 53248 that allows: at d_model <= 2048 any batch; at
+ *   d_model 4096 a batch of at most 2 tokens (a 3-token or larger batch takes 4-token tiles,
+ *   about 9.7 MB); at d_model 8192 a single token. Larger requests return
  *   PROX_ERR_WORKSPACE before anything is launched.
  *   Set-up: the first call on each device looks up the array's device address (with that
  *   device current) and caches it; make that first call before any stream capture.
@@ -192,6 +197,12 @@ const char* prox_error_string(int code);
  * library was doing and the runtime's error name and text ("none" if there was none).
  * Thread-local storage, valid until the thread's next failing call. */
 const char* prox_last_cuda_error(void);
+
+/* Number of kernel launches the library has enqueued in this process so far, on any thread
+ * and device. A launch recorded into a CUDA graph under stream capture counts once, when it is
+ * recorded (graph replays do not call the library). Memory copies and memsets are not kernel
+ * launches of the library and are not counted. */
+uint64_t prox_launch_count(void);
 
 /* Test hook: the same input-selection and Stage-1 kernels as prox_build_mask, also storing
  * the exact integer intermediates (technical summary, Stage 1 "Proxy Activation").

@@ -54,7 +54,9 @@ def decode_packed(buf: np.ndarray, d: int, F: int) -> dict:
 
 def check_band(sigma: np.ndarray, k: int, idx) -> None:
     """GPU mask vs the oracle salience: exactly k ascending channels, containing every
-    channel clearly above the k-th oracle value and none clearly below it."""
+    channel clearly above the k-th oracle value and none clearly below it. Among the
+    channels whose oracle salience equals the k-th value exactly, the ones taken must be the
+    lowest indices (the ranking rule gives equal values to the lower channel index)."""
     idx = np.asarray(idx, dtype=np.int64)
     assert len(idx) == k
     assert np.all(np.diff(idx) > 0), "mask not strictly ascending"
@@ -65,6 +67,12 @@ def check_band(sigma: np.ndarray, k: int, idx) -> None:
     must_not = set(np.nonzero(sigma < sk * (1 - BAND))[0].tolist())
     assert must <= got, f"missing {len(must - got)} channels above the band"
     assert not (must_not & got), f"{len(must_not & got)} channels below the band selected"
+    ties = np.nonzero(sigma == sk)[0]          # ascending
+    if len(ties) > 1:
+        taken = np.array([j in got for j in ties.tolist()])
+        n = int(taken.sum())
+        assert taken[:n].all() and not taken[n:].any(), \
+            "equal saliences not taken lowest index first"
 
 
 def check_y(y_gpu: np.ndarray, y_ref: np.ndarray) -> None:

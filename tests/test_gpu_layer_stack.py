@@ -54,3 +54,28 @@ def test_stack_llama3_8b_layers():
     layers = [Layer(WL.make_layer(4, li)) for li in range(3)]
     x0 = WL.make_tokens(4, [0])
     _run_chain(layers, x0, 0.7, 0.5)
+
+
+def test_stack_llama3_8b_all_32_layers():
+    """The whole 32-layer 4096 x 14336 stack for one token: each layer is built, run from the
+    previous layer's GPU output, checked against the oracle and released before the next one,
+    so host and device memory hold one layer at a time."""
+    k = O.k_for(0.7, 14336)
+    ws = P.prox_workspace(4096, 14336, 1)
+    x = cuda(WL.make_tokens(4, [1]))
+    for li in range(32):
+        lay = Layer(WL.make_layer(4, li))
+        idx = torch.empty((1, k), dtype=torch.int32, device="cuda")
+        y = P.prox_ffn_forward(lay.packed, x, 0.7, 0.5, ws, idx_out=idx)
+        x_next = P.prox_rmsnorm(y, 1e-6)
+        assert P.prox_get_status(ws) == 0
+        xin = x.cpu().numpy()[0]
+        idx_h = idx.cpu().numpy()[0]
+        check_band(O.stage1_token(lay.o, xin, 0.5)["sigma"], k, idx_h)
+        y_ref, _ = O.stage2_exact(xin, lay.o.w_gate, lay.o.w_up, lay.o.w_down, idx_h)
+        y_h = y.cpu().numpy()[0]
+        check_y(y_h, y_ref)
+        np.testing.assert_allclose(x_next.cpu().numpy()[0], O.rmsnorm(y_h[None], 1e-6)[0],
+                                   rtol=2e-6, atol=1e-7)
+        x = x_next
+        del lay

@@ -245,7 +245,7 @@ def test_host_entry_point():
 
 # ----------------------------------------------------------------------------- full sizes
 
-@pytest.mark.parametrize("batch", [1, 16])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8, 16])
 def test_llama3_8b_layer_full_size(batch):
     """The benchmarked layer (4096 x 14336, 70% channel / 50% input sparsity), checked on
     sampled tokens of the batch one by one."""
@@ -293,3 +293,36 @@ def test_llama2_70b_batch8_full_size():
         check_band(st["sigma"], k, idx[b])
         y_ref, _ = O.stage2_exact(x[b], lay.o.w_gate, lay.o.w_up, lay.o.w_down, idx[b])
         check_y(y[b], y_ref)
+
+
+def test_channel_permutation_equivariance():
+    """Renumbering the intermediate channels (rows of W_gate and W_up, columns of W_down, by
+    one permutation) renumbers the salience, the mask and nothing else: the salience of a
+    channel does not depend on its position (bitwise), the mask is the renumbered mask, and y
+    is unchanged up to the order of the fp32 sums."""
+    d, F = 1024, 2816
+    mats = WL.make_random_layer(d, F, seed=24)
+    perm = np.random.default_rng(25).permutation(F)
+    inv = np.argsort(perm)
+    pm = {"w_gate": mats["w_gate"][torch.from_numpy(perm)].contiguous(),
+          "w_up": mats["w_up"][torch.from_numpy(perm)].contiguous(),
+          "w_down": mats["w_down"][:, torch.from_numpy(perm)].contiguous()}
+    from gpu_helpers import Layer
+    lay, lay_p = Layer(mats), Layer(pm)
+    ws = ws_for(lay, 1)
+    x = _tokens(1, d, seed=26)
+    s = P.prox_debug_stage1(lay.packed, cuda(x), 0.5, ws)["salience"].cpu().numpy()[0]
+    s_p = P.prox_debug_stage1(lay_p.packed, cuda(x), 0.5, ws)["salience"].cpu().numpy()[0]
+    np.testing.assert_array_equal(s_p, s[perm])
+    k = O.k_for(0.7, F)
+    idx = P.prox_build_mask(lay.packed, cuda(x), 0.7, 0.5, ws).cpu().numpy()[0]
+    idx_p = P.prox_build_mask(lay_p.packed, cuda(x), 0.7, 0.5, ws).cpu().numpy()[0]
+    if len(np.unique(s)) == F:   # no exact ties: the renumbered mask is unique
+        np.testing.assert_array_equal(idx_p, np.sort(inv[idx]))
+    y = P.prox_ffn_forward(lay.packed, cuda(x), 0.7, 0.5, ws).cpu().numpy()[0]
+    y_p = P.prox_ffn_forward(lay_p.packed, cuda(x), 0.7, 0.5, ws).cpu().numpy()[0]
+    assert P.prox_get_status(ws) == 0
+    check_y(y_p, y)
+    y_ref, _ = O.stage2_exact(x[0], lay.o.w_gate, lay.o.w_up, lay.o.w_down, idx)
+    check_y(y_p, y_ref)
+    assert len(idx) == k

@@ -5,14 +5,18 @@ allowed or not affordable (a serving runtime that reserved all device memory for
 pool, a latency-critical loop that cannot take cudaMalloc's implicit synchronization). For
 them the library keeps the Stage-2 scratch in a fixed device array of its own. These tests
 call that entry point through the C ABI twice in a row, with different inputs each time, and
-check every output against the workspace entry point within the Stage-2 tolerance; and they
-check that a request larger than the fixed array is refused before anything is launched.
+check every output against the workspace entry point and against the oracle's exact Stage 2
+over the same mask, within the Stage-2 tolerance. Batches larger than one token tile (6 and 9
+tokens at d_model 1024, tiles of 4) run several tiles one after another through the same
+shared array. A request larger than the fixed array must be refused before anything is
+launched.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle as O
 import workloads as WL
 import free_sparse_swiglu_stage1_b300 as P
 from free_sparse_swiglu_stage1_b300 import _lib
@@ -21,7 +25,8 @@ from gpu_helpers import check_y, cuda, random_layer, ws_for
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("d,F,batch", [(1024, 2816, 1), (4096, 1024, 1), (1024, 2816, 2)])
+@pytest.mark.parametrize("d,F,batch", [(1024, 2816, 1), (4096, 1024, 1), (1024, 2816, 2),
+                                       (1024, 2816, 6), (1024, 2816, 9)])
 def test_noalloc_matches_workspace_entry_point(d, F, batch):
     lay = random_layer(d, F, seed=d + F + batch)
     ws = ws_for(lay, batch)
@@ -39,8 +44,11 @@ def test_noalloc_matches_workspace_entry_point(d, F, batch):
         assert rc == 0, P.prox_error_string(rc)
         assert status.value == 0, P.prox_error_string(status.value)
         got, ref = y.cpu().numpy(), y_ref.cpu().numpy()
+        xh, idxh = x.cpu().numpy(), idx.cpu().numpy()
         for b in range(batch):
             check_y(got[b], ref[b])
+            y_o, _ = O.stage2_exact(xh[b], lay.o.w_gate, lay.o.w_up, lay.o.w_down, idxh[b])
+            check_y(got[b], y_o)
     assert P.prox_get_status(ws) == 0
 
 
