@@ -25,6 +25,11 @@ class ProxError(RuntimeError):
         super().__init__(f"{where}: {error_string(code)} ({code}){detail}")
 
 
+class prox_cost_model(ctypes.Structure):
+    _fields_ = [("in_cost", ctypes.c_double), ("fixed_cost", ctypes.c_double),
+                ("ch_cost", ctypes.c_double), ("dense_cost", ctypes.c_double)]
+
+
 class prox_packed(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("group", ctypes.c_int32), ("reserved", ctypes.c_int32),
@@ -40,6 +45,9 @@ SIGNATURES = {
     "prox_workspace_bytes": (_sz, [_i, _i, _i]),
     "prox_workspace_init": (_i, [_vp, _sz, _vp]),
     "prox_k_for": (_i, [_d, _i]),
+    "prox_cost_model_bytes": (_i, [_i, _i, ctypes.POINTER(prox_cost_model)]),
+    "prox_choose_sparsity": (_i, [ctypes.POINTER(prox_cost_model), _i, _i, _d, _d, _d, _vp, _vp,
+                                  _vp]),
     "prox_pack_weights": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _P]),
     "prox_build_mask": (_i, [_P, _vp, _i, _d, _d, _vp, _vp, _sz, _vp]),
     "prox_sparse_ffn": (_i, [_P, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp]),

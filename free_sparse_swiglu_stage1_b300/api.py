@@ -12,7 +12,7 @@ from dataclasses import dataclass
 import torch
 
 from . import _lib
-from ._lib import ProxError, prox_packed
+from ._lib import ProxError, prox_cost_model, prox_packed
 
 GROUP = 128
 MAX_BATCH = 16
@@ -46,6 +46,25 @@ def prox_workspace_bytes(d_model: int, d_ff: int, batch: int) -> int:
 
 def prox_k_for(sparsity: float, n: int) -> int:
     return int(_lib.lib().prox_k_for(float(sparsity), int(n)))
+
+
+def prox_cost_model_bytes(d_model: int, d_ff: int) -> prox_cost_model:
+    """The HBM-byte cost model of a layer shape (see include/prox.h)."""
+    out = prox_cost_model()
+    _lib.check(_lib.lib().prox_cost_model_bytes(d_model, d_ff, ctypes.byref(out)),
+               "prox_cost_model_bytes")
+    return out
+
+
+def prox_choose_sparsity(cost: prox_cost_model, d_model: int, d_ff: int, target: float,
+                         anchor: float = 0.7, min_input_kept: float = 0.3):
+    """(input_sparsity, sparsity, effective_sparsity) for a target effective sparsity."""
+    s1, s2, eff = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _lib.check(_lib.lib().prox_choose_sparsity(ctypes.byref(cost), d_model, d_ff, float(target),
+                                               float(anchor), float(min_input_kept),
+                                               ctypes.byref(s1), ctypes.byref(s2),
+                                               ctypes.byref(eff)), "prox_choose_sparsity")
+    return s1.value, s2.value, eff.value
 
 
 @dataclass
@@ -312,6 +331,7 @@ def prox_debug_wait_timeout(ws: Workspace, spin_cycles: int, stream=None) -> Non
 
 __all__ = [
     "GROUP", "MAX_BATCH", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
+    "prox_choose_sparsity", "prox_cost_model", "prox_cost_model_bytes",
     "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",
     "prox_launch_count",

@@ -139,6 +139,31 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
     uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
     const bool tc = y && !dbg && use_tc(w, B, W, sms);
+    if (B == 1 && !g_fused_sel && fused_supported(d, F, sms)) {
+        // one token: the whole path in one persistent launch
+        FusedCall c;
+        c.x = x;
+        c.k = k;
+        c.k_in = k_in;
+        c.sigma = sigma;
+        if (all_channels) {
+            if (idx_out) PROX_TRY(launch_iota(idx, F, B, s));
+            if (!y) return PROX_OK;
+            c.mode = kFusedStage2 | kFusedDense;
+        } else if (dbg) {
+            c.mode = kFusedStage1;
+            c.dbg_qx = dbg->qx;
+            c.dbg_sx = dbg->sx;
+            c.dbg_gate = dbg->acc_gate;
+            c.dbg_up = dbg->acc_up;
+        } else {
+            c.mode = kFusedStage1 | kFusedSelect | (y ? kFusedStage2 : 0);
+            c.idx = idx;
+            c.write_idx = idx_out != nullptr;
+        }
+        c.y = y;
+        return launch_fused(packed, L, d, F, c, ws, W, sms, s);
+    }
     if (all_channels) {
         // sparsity 0: every channel is kept, the ranking cannot change the result
         if (idx_out) PROX_TRY(launch_iota(idx, F, B, s));
@@ -207,6 +232,58 @@ int prox_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     return cuda_ok(cudaMemsetAsync(ws, 0, n, static_cast<cudaStream_t>(stream)), "clearing the workspace");
 }
 
+int prox_cost_model_bytes(int d_model, int d_ff, prox_cost_model* out) {
+    if (!out || !shape_ok(d_model, d_ff)) return PROX_ERR_INVALID_ARG;
+    const double d = d_model, F = d_ff, G = d_model / 128;
+    out->in_cost = F;
+    out->fixed_cost = 4.0 * G * F;
+    out->ch_cost = 6.0 * d;
+    out->dense_cost = 6.0 * d * F;
+    return PROX_OK;
+}
+
+int prox_choose_sparsity(const prox_cost_model* cost, int d_model, int d_ff, double target,
+                         double anchor, double min_input_kept, double* input_sparsity,
+                         double* sparsity, double* effective) {
+    if (!cost || d_model < 1 || d_ff < 1) return PROX_ERR_INVALID_ARG;
+    if (!(cost->in_cost > 0.0) || !(cost->ch_cost > 0.0) || !(cost->dense_cost > 0.0) ||
+        !(cost->fixed_cost >= 0.0))
+        return PROX_ERR_INVALID_ARG;
+    if (!(target >= 0.0 && target < 1.0) || !sparsity_ok(anchor) ||
+        !(min_input_kept > 0.0 && min_input_kept <= 1.0))
+        return PROX_ERR_INVALID_ARG;
+    const int d = d_model, F = d_ff;
+    const double budget = (1.0 - target) * cost->dense_cost;
+    long long k_in_min = static_cast<long long>(std::ceil(min_input_kept * d));
+    if (k_in_min < 1) k_in_min = 1;
+    if (k_in_min > d) k_in_min = d;
+    const long long k_anchor = k_rule(anchor, F);
+    double v = std::floor((budget - cost->fixed_cost - cost->ch_cost * static_cast<double>(k_anchor)) /
+                          cost->in_cost);
+    long long k_in, k;
+    if (v >= d) {
+        k_in = d;
+        const double kk = std::floor((budget - cost->fixed_cost - cost->in_cost * static_cast<double>(d)) /
+                                     cost->ch_cost);
+        k = kk >= F ? F : static_cast<long long>(kk);
+    } else if (v >= static_cast<double>(k_in_min)) {
+        k_in = static_cast<long long>(v);
+        k = k_anchor;
+    } else {
+        k_in = k_in_min;
+        const double kk = std::floor((budget - cost->fixed_cost - cost->in_cost * static_cast<double>(k_in)) /
+                                     cost->ch_cost);
+        if (kk < 1.0) return PROX_ERR_UNSUPPORTED;
+        k = static_cast<long long>(kk);
+    }
+    const double c = (cost->in_cost * static_cast<double>(k_in) + cost->fixed_cost +
+                      cost->ch_cost * static_cast<double>(k)) / cost->dense_cost;
+    if (input_sparsity) *input_sparsity = 1.0 - static_cast<double>(k_in) / d;
+    if (sparsity) *sparsity = 1.0 - static_cast<double>(k) / F;
+    if (effective) *effective = 1.0 - c;
+    return PROX_OK;
+}
+
 int prox_k_for(double sparsity, int n) {
     if (!sparsity_ok(sparsity) || n < 1) return -1;
     return k_rule(sparsity, n);
@@ -259,6 +336,16 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
+    if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
+        FusedCall c;
+        c.x = x;
+        c.k = k;
+        c.idx_in = idx;
+        c.y = y;
+        c.mode = kFusedStage2 | kFusedGiven;
+        return launch_fused(static_cast<const uint8_t*>(w->base), L, d, w->d_ff, c,
+                            static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream));
+    }
     if (use_tc(w, batch, W, sms))
         return run_stage2_tc(w, L, x, batch, idx, k, nullptr, y, static_cast<uint8_t*>(ws), W,
                              sms, static_cast<cudaStream_t>(stream));
@@ -319,6 +406,15 @@ int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, vo
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
     const PackedLayout L = packed_layout(w->d_model, w->d_ff);
     const int d = w->d_model;
+    if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
+        FusedCall c;
+        c.x = x;
+        c.k = w->d_ff;
+        c.y = y;
+        c.mode = kFusedStage2 | kFusedDense;
+        return launch_fused(static_cast<const uint8_t*>(w->base), L, d, w->d_ff, c,
+                            static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream));
+    }
     if (use_tc(w, batch, W, sms))
         return run_stage2_tc(w, L, x, batch, nullptr, w->d_ff, nullptr, y,
                              static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream));

@@ -184,6 +184,21 @@ __host__ __device__ inline int select_run(int n, int nt) {
     return r;
 }
 
+// The uint4 slot that holds the i4-th group of 4 keys of thread t's run of RUN keys. Plain:
+// t * RUN / 4 + i4 (runs contiguous). Swizzled (SWZ): the slot inside the run is XORed with a
+// function of t chosen so that the threads of a warp reading their i4-th groups at once touch
+// different bank groups (contiguous runs of 32 or more bytes per thread otherwise conflict).
+template <int RUN, bool SWZ>
+__device__ __forceinline__ int key_quad(int t, int i4) {
+    constexpr int R4 = RUN / 4;
+    if constexpr (!SWZ || R4 == 1) {
+        return t * R4 + i4;
+    } else {
+        const int s = R4 >= 8 ? (t & 7) : ((t * R4 / 8) & (R4 - 1));
+        return t * R4 + (i4 ^ s);
+    }
+}
+
 // Over the bins of histogram h taken in descending order, finds the bin where the running
 // count reaches `remaining` (1 <= remaining <= total). Writes sel[0] = that bin, sel[1] = the
 // count in the bins above it, sel[2] = the count in the bin. nbins <= 2048, a multiple of NT
@@ -229,15 +244,17 @@ __device__ __forceinline__ void block_find_bin(const int* h, int nbins, int rema
     __syncthreads();
 }
 
-// Radix select over n keys (bit 31 clear, n a multiple of 4) held in shared memory, in three
-// passes of 11, 11 and 9 bits. Thread t scans the run [t*RUN, t*RUN + RUN). Finds T, the k-th
-// largest key (1 <= k <= n); take_eq, how many keys equal to T belong to the top k when ties
-// go to the lowest indices; and eq_total, how many keys equal T. `hist` is 2 * 2048 ints and
+// Radix select over n keys (bit 31 clear, n a multiple of 4) held in shared memory, in up to
+// three passes of 11, 11 and 9 bits. Thread t scans the run [t*RUN, t*RUN + RUN). Finds T, the
+// k-th largest key (1 <= k <= n); take_eq, how many keys equal to T belong to the top k when
+// ties go to the lowest indices; and eq_total, how many keys equal T. If a pass finds that the
+// bin holding the k-th key is taken whole, it stops there: T is then the bin's lowest value
+// and take_eq = eq_total = 2^30, so "key > T, or key == T" selects exactly the top k. `hist` is 2 * 2048 ints and
 // `wsum` NT/32 + 4 ints of shared memory. If hist0 is not null it holds the first pass's
 // 2048-bin histogram of the keys' bits 30..20 (built by whoever produced the keys), and that
 // pass only reads it.
 // If hist_ready, hist[0, 2048) already holds that first-pass histogram in shared memory.
-template <int NT, int RUN>
+template <int NT, int RUN, bool SWZ = false>
 __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, int* wsum,
                                  uint32_t& T, int& take_eq, int& eq_total,
                                  const int* hist0 = nullptr, bool hist_ready = false) {
@@ -263,7 +280,7 @@ __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, 
 #pragma unroll
             for (int i4 = 0; i4 < RUN / 4; ++i4) {
                 if (4 * i4 < nv) {
-                    const uint4 kk = *reinterpret_cast<const uint4*>(keys + lo + 4 * i4);
+                    const uint4 kk = reinterpret_cast<const uint4*>(keys)[key_quad<RUN, SWZ>(tid, i4)];
                     const uint32_t k4[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
                     for (int m = 0; m < 4; ++m)
@@ -282,6 +299,13 @@ __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, 
         eq_total = sel[2];
         prefix |= dig << shift;
         pmask |= dmask << shift;
+        if (p < 2 && eq_total == remaining) {
+            // the whole bin is taken: every key >= the bin's lowest value is in the top k
+            T = prefix;
+            take_eq = eq_total = 1 << 30;
+            __syncthreads();
+            return;
+        }
     }
     T = prefix;
     take_eq = remaining;
@@ -292,7 +316,7 @@ __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, 
 // is above T, or equal to T and among the first take_eq equal keys in index order. Thread t
 // owns the run [t*RUN, t*RUN + RUN) (RUN <= 64); `take` receives one bit per element of the
 // run. Returns the number taken in the run. `wsum` as for the scan.
-template <int NT, int RUN>
+template <int NT, int RUN, bool SWZ = false>
 __device__ __forceinline__ int block_take_topk(const uint32_t* keys, int n, uint32_t T,
                                                int take_eq, int eq_total, int* wsum,
                                                uint64_t& take) {
@@ -303,7 +327,7 @@ __device__ __forceinline__ int block_take_topk(const uint32_t* keys, int n, uint
         int eq = 0;
 #pragma unroll
         for (int i = 0; i < RUN; ++i)
-            if (i < nv) eq += keys[lo + i] == T;
+            if (i < nv) eq += keys[4 * key_quad<RUN, SWZ>(threadIdx.x, i >> 2) + (i & 3)] == T;
         int eq_all;
         e = block_exclusive_scan<NT>(eq, wsum, eq_all);
     }
@@ -312,7 +336,7 @@ __device__ __forceinline__ int block_take_topk(const uint32_t* keys, int n, uint
 #pragma unroll
     for (int i4 = 0; i4 < RUN / 4; ++i4) {
         if (4 * i4 < nv) {
-            const uint4 kk = *reinterpret_cast<const uint4*>(keys + lo + 4 * i4);
+            const uint4 kk = reinterpret_cast<const uint4*>(keys)[key_quad<RUN, SWZ>(threadIdx.x, i4)];
             const uint32_t k4[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {

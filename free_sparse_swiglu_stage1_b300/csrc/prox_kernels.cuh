@@ -87,10 +87,30 @@ inline int tc_blocks(int F, int sms) {
     return sms > need ? sms : need;
 }
 
+// ------------------------------------------------------------------ fused single-token path
+// One persistent launch of one block per SM runs the whole single-token path (input selection,
+// Stage 1, top-k, Stage 2, the cross-block sum) with grid-wide barriers between the steps that
+// exchange data across blocks. Block p owns a tile of at most kFusedTileMax channels in Stage 1.
+constexpr int kFusedThreads = 512;
+constexpr int kFusedMaxBlocks = 256;
+constexpr int kFusedTileMax = 256;
+struct GridBarrier {
+    unsigned long long arrived;   // total block arrivals over every barrier so far (only grows)
+};
+// Lives in the cleared control region of a workspace: prox_workspace_init zeroes it and every
+// fused launch leaves the histogram zeroed again for the next one.
+struct FusedControl {
+    GridBarrier bar;
+    int pad[6];
+    unsigned readers;   // blocks that read the histogram in a launch without a later barrier
+    int pad2[3];
+    int hist[2048];     // the layer's salience histogram over bits 30..20 (count per bin)
+};
+
 // ------------------------------------------------------------------ workspace layout
 struct WsLayout {
-    size_t control, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, qxh, sigma, idx, ulist, ubits,
-        xhl, ypart, total;
+    size_t control, fctl, xbuf, ybuf, grows, gqx, gcnt, gq, sx, ghist, qxh, sigma, idx, ulist,
+        ubits, xhl, ypart, total;
     int TB, P, BPtc;
 };
 
@@ -111,6 +131,7 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     W.control = take(sizeof(Control));
+    W.fctl = take(sizeof(FusedControl));
     W.xbuf = take(static_cast<size_t>(B) * d * 4);
     W.ybuf = take(static_cast<size_t>(B) * d * 4);
     const size_t nt = static_cast<size_t>(token_tiles(B, W.TB));   // per-tile buffers below
@@ -134,8 +155,9 @@ inline WsLayout ws_layout(int d, int F, int B, int sms) {
     return W;
 }
 
-// Bytes of the control region that prox_workspace_init clears.
-inline size_t ws_control_bytes() { return align_up(sizeof(Control)); }
+// Bytes of the control region that prox_workspace_init clears (the control block and the
+// fused path's barrier and histogram, which follow it).
+inline size_t ws_control_bytes() { return align_up(sizeof(Control)) + align_up(sizeof(FusedControl)); }
 
 // ------------------------------------------------------------------ launches
 // Records a failed CUDA call (the error and what was being done) for prox_last_cuda_error;
@@ -248,6 +270,35 @@ int launch_stage2_select(const uint8_t* packed, const PackedLayout& L, int d, in
                          const float* x, const float* sigma, const int* ghist, int k, float* y,
                          int32_t* dbg_sel, uint8_t* ws, const WsLayout& W, int sms,
                          cudaStream_t s);
+
+// The fused single-token path. mode is a set of FusedMode bits:
+//   kFusedStage1  input selection, Stage-1 GEMV, salience (into sigma)
+//   kFusedSelect  top-k of the salience into idx (ascending)
+//   kFusedStage2  Stage 2 + cross-block sum into y, over the mask from kFusedSelect, or over
+//                 every channel (kFusedDense), or over idx_in (kFusedGiven)
+enum FusedMode : int {
+    kFusedStage1 = 1,
+    kFusedSelect = 2,
+    kFusedStage2 = 4,
+    kFusedDense = 8,
+    kFusedGiven = 16,
+};
+struct FusedCall {
+    const float* x = nullptr;
+    int k = 0, k_in = 0, mode = 0;
+    const int32_t* idx_in = nullptr;   // kFusedGiven: [k] ascending
+    int32_t* idx = nullptr;            // kFusedSelect: [k] ascending mask
+    bool write_idx = false;            // store the mask into idx (else only used in-kernel)
+    float* sigma = nullptr;            // kFusedStage1: [F] written
+    float* y = nullptr;                // kFusedStage2: [d] written
+    int8_t* dbg_qx = nullptr;          // Stage-1 intermediates (test hook), each nullable
+    float* dbg_sx = nullptr;
+    int32_t* dbg_gate = nullptr;
+    int32_t* dbg_up = nullptr;
+};
+bool fused_supported(int d, int F, int sms);
+int launch_fused(const uint8_t* packed, const PackedLayout& L, int d, int F, const FusedCall& c,
+                 uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s);
 
 int launch_rmsnorm(const float* y, float* x_out, int batch, int d, float eps, cudaStream_t s);
 

@@ -73,6 +73,42 @@ typedef struct prox_packed {
     size_t  bytes;
 } prox_packed;
 
+/* Cost model of one layer for prox_choose_sparsity: per token, the sparse path costs
+ *   in_cost * k_in + fixed_cost + ch_cost * k
+ * (k_in kept inputs, k selected channels) and the dense FFN dense_cost, in any one unit
+ * (bytes of HBM traffic, or measured microseconds). */
+typedef struct prox_cost_model {
+    double in_cost;      /* per kept input (Stage 1 reads one proxy row)                    */
+    double fixed_cost;   /* independent of the sparsities (proxy scales, selections)        */
+    double ch_cost;      /* per selected channel (Stage 2 reads three bf16 rows)            */
+    double dense_cost;   /* the dense SwiGLU FFN of the same layer                          */
+} prox_cost_model;
+
+/* The HBM-byte cost model of a layer shape: in_cost = d_ff (one byte of INT4 gate+up codes
+ * per channel), fixed_cost = 4 * (d_model / 128) * d_ff (fp16 scales of both proxies),
+ * ch_cost = 6 * d_model, dense_cost = 6 * d_model * d_ff. PROX_ERR_INVALID_ARG for a bad
+ * shape or a NULL out. */
+int prox_cost_model_bytes(int d_model, int d_ff, prox_cost_model* out);
+
+/* Sparsity allocation (technical summary, "Sparsity Allocation": the Stage 2 sparsity is
+ * anchored around 70%, Stage 1 keeps at least 30% of the inputs, and a cost model chooses the
+ * two sparsities for a target effective sparsity, counting the proxy's overhead). The pages
+ * give no formula; this call implements the following reading.
+ *   Effective sparsity = 1 - C, with C = (in_cost k_in + fixed_cost + ch_cost k) / dense_cost
+ *   the sparse path's cost relative to the dense FFN. For `target` in [0, 1), the budget is
+ *   C <= 1 - target. Rule: keep k = prox_k_for(anchor, d_ff) channels and the most inputs
+ *   the budget allows; if that is every input, keep every input and the most channels that
+ *   fit; if it is fewer than ceil(min_input_kept * d_model), keep that many inputs and the
+ *   most channels that fit.
+ *   Outputs (any may be NULL): input_sparsity = 1 - k_in / d_model and sparsity =
+ *   1 - k / d_ff (prox_k_for maps them back to k_in and k), effective = 1 - C.
+ * Host-only: launches nothing. PROX_ERR_INVALID_ARG for bad arguments (costs must be
+ * positive, 0 <= anchor < 1, 0 < min_input_kept <= 1), PROX_ERR_UNSUPPORTED if no allocation
+ * fits the budget. */
+int prox_choose_sparsity(const prox_cost_model* cost, int d_model, int d_ff, double target,
+                         double anchor, double min_input_kept, double* input_sparsity,
+                         double* sparsity, double* effective);
+
 /* Bytes prox_pack_weights needs for one layer; 0 if the shape is invalid. */
 size_t prox_packed_bytes(int d_model, int d_ff, int group);
 
