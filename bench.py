@@ -63,6 +63,8 @@ def parse(argv=None):
     ap.add_argument("--tokens", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="Stage-2 rows as FP8 E4M3 with row scales (single token only)")
     ap.add_argument("--spread-ms", type=float, default=300.0,
                     help="wall time of the extra chunked run that gives the p10/p50/p90 spread")
     return ap.parse_args(argv)
@@ -104,17 +106,20 @@ def resolve(args) -> dict:
     s_in = args.input_sparsity if args.input_sparsity is not None else w.input_sparsity
     chain = args.workload == CHAIN_WORKLOAD
     d, F = w.d_model, w.d_ff
-    packed = d * F + 4 * (d // 128) * F + 6 * F * d
+    packed = d * F + 4 * (d // 128) * F + (3 * d + 16 if getattr(args, "fp8", False) else 6 * d) * F
     if chain:
         layers = w.layers
     elif args.layers is not None:
         layers = args.layers
     else:
         layers = max(4, math.ceil(3 * L2_BYTES / packed))
-    name = (f"{w.name}-b{batch}-s{round(sp * 100)}-in{round(s_in * 100)}")
+    name = (f"{w.name}-b{batch}-s{round(sp * 100)}-in{round(s_in * 100)}"
+            + ("-fp8" if getattr(args, "fp8", False) else ""))
+    row = 3 * d + 16 if getattr(args, "fp8", False) else 6 * d
     return {"key": args.workload, "name": name, "d": d, "F": F, "batch": batch,
             "sparsity": sp, "input_sparsity": s_in, "layers": layers, "chain": chain,
-            "depth": w.layers if chain else 1, "packed_bytes": packed}
+            "depth": w.layers if chain else 1, "packed_bytes": packed, "row_bytes": row,
+            "fp8": bool(getattr(args, "fp8", False))}
 
 
 def workload_config(cfg: dict, world: int, tokens: int, k: int, k_in: int) -> dict:
@@ -134,17 +139,20 @@ def workload_config(cfg: dict, world: int, tokens: int, k: int, k_in: int) -> di
     return c
 
 
-def algorithmic_bytes(d, F, k_in_rows, k_rows, batch):
+def algorithmic_bytes(d, F, k_in_rows, k_rows, batch, row_bytes=None):
     """Bytes the method must move per layer pass: kept int4 proxy rows (gate+up, one byte per
-    channel), fp16 group scales of both proxies, the selected bf16 rows of W_gate, W_up and
-    W_down^T, plus x, y, the mask and the salience."""
+    channel), fp16 group scales of both proxies, the selected channels' Stage-2 rows (bf16
+    W_gate, W_up and W_down^T rows: 6 d bytes; FP8 rows with scales: 3 d + 16), plus x, y,
+    the mask and the salience."""
     G = d // 128
-    return (k_in_rows * F + 4 * G * F + 6 * k_rows * d
+    rb = 6 * d if row_bytes is None else row_bytes
+    return (k_in_rows * F + 4 * G * F + rb * k_rows
             + batch * (8 * d + 8 * F) + 4 * batch * k_rows)
 
 
-def stage2_bytes(d, k_rows, batch):
-    return 6 * k_rows * d + batch * 8 * d + 4 * batch * k_rows
+def stage2_bytes(d, k_rows, batch, row_bytes=None):
+    rb = 6 * d if row_bytes is None else row_bytes
+    return rb * k_rows + batch * 8 * d + 4 * batch * k_rows
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -418,7 +426,8 @@ def run_ours(args):
         if li == 0:
             mats0 = mats
         dev = {n: v.cuda() for n, v in mats.items() if n.startswith("w_")}
-        layers.append(P.prox_pack_weights(dev["w_gate"], dev["w_up"], dev["w_down"]))
+        layers.append(P.prox_pack_weights(dev["w_gate"], dev["w_up"], dev["w_down"],
+                                          fp8=cfg["fp8"]))
         del dev
     torch.cuda.synchronize()
     X_np = WL.make_tokens(cfg["key"], range(rank * T, (rank + 1) * T))
@@ -610,8 +619,8 @@ def run_ours(args):
             kept_sizes.append(len(kept))
         union_sizes = [len(np.unique(it[2].cpu().numpy())) for it in s2_items]
         rows_in, rows_ch = statistics.mean(kept_sizes), statistics.mean(union_sizes)
-    path_bytes = algorithmic_bytes(d, F, rows_in, rows_ch, B) * depth
-    s2_bytes = stage2_bytes(d, rows_ch, B)
+    path_bytes = algorithmic_bytes(d, F, rows_in, rows_ch, B, cfg["row_bytes"]) * depth
+    s2_bytes = stage2_bytes(d, rows_ch, B, cfg["row_bytes"])
 
     peaks = {}
     try:
@@ -662,7 +671,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": warm, "ms_per_step": 1000.0 * s_fwd,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": "fp8-e4m3 Stage-2 weights" if cfg["fp8"] else "bf16", "data": "synthetic",
         "config": workload_config(cfg, world, T, k, k_in),
         "us_per_layer": us_layer,
         "us_per_step_chunks": fwd_stats,

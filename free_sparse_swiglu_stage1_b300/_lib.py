@@ -32,7 +32,7 @@ class prox_cost_model(ctypes.Structure):
 
 class prox_packed(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("format", ctypes.c_int32),
                 ("base", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
@@ -49,6 +49,8 @@ SIGNATURES = {
     "prox_choose_sparsity": (_i, [ctypes.POINTER(prox_cost_model), _i, _i, _d, _d, _d, _vp, _vp,
                                   _vp]),
     "prox_pack_weights": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _P]),
+    "prox_pack_weights_fp8": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _sz, _vp, _P]),
+    "prox_packed_bytes_fp8": (_sz, [_i, _i, _i]),
     "prox_build_mask": (_i, [_P, _vp, _i, _d, _d, _vp, _vp, _sz, _vp]),
     "prox_sparse_ffn": (_i, [_P, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp]),
     "prox_ffn_forward": (_i, [_P, _vp, _i, _d, _d, _vp, _vp, _vp, _sz, _vp]),

@@ -36,8 +36,16 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: int | None = None
     return t.data_ptr()
 
 
+FORMAT_BF16 = 0
+FORMAT_FP8 = 1
+
+
 def prox_packed_bytes(d_model: int, d_ff: int, group: int = GROUP) -> int:
     return int(_lib.lib().prox_packed_bytes(d_model, d_ff, group))
+
+
+def prox_packed_bytes_fp8(d_model: int, d_ff: int, group: int = GROUP) -> int:
+    return int(_lib.lib().prox_packed_bytes_fp8(d_model, d_ff, group))
 
 
 def prox_workspace_bytes(d_model: int, d_ff: int, batch: int) -> int:
@@ -115,21 +123,23 @@ def prox_workspace_init(ws: Workspace, stream=None) -> None:
 
 
 def prox_pack_weights(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Tensor,
-                      group: int = GROUP, stream=None) -> PackedLayer:
+                      group: int = GROUP, stream=None, fp8: bool = False) -> PackedLayer:
+    """Packs one layer; with fp8 the Stage-2 rows are kept as FP8 E4M3 with row scales
+    (prox_pack_weights_fp8)."""
     F, d = w_gate.shape
     if tuple(w_up.shape) != (F, d) or tuple(w_down.shape) != (d, F):
         raise ValueError("expected w_gate, w_up [d_ff, d_model] and w_down [d_model, d_ff]")
     pg = _dev(w_gate, torch.bfloat16, "w_gate", 2)
     pu = _dev(w_up, torch.bfloat16, "w_up", 2)
     pd = _dev(w_down, torch.bfloat16, "w_down", 2)
-    n = prox_packed_bytes(d, F, group)
+    n = (prox_packed_bytes_fp8 if fp8 else prox_packed_bytes)(d, F, group)
     if n == 0:
         raise ValueError(f"unsupported layer shape d_model={d}, d_ff={F}")
     buf = torch.empty(n, dtype=torch.uint8, device=w_gate.device)
     desc = prox_packed()
-    _lib.check(_lib.lib().prox_pack_weights(pg, pu, pd, d, F, group, buf.data_ptr(), n,
-                                            _stream(stream, w_gate.device), ctypes.byref(desc)),
-               "prox_pack_weights")
+    name = "prox_pack_weights_fp8" if fp8 else "prox_pack_weights"
+    _lib.check(getattr(_lib.lib(), name)(pg, pu, pd, d, F, group, buf.data_ptr(), n,
+                                         _stream(stream, w_gate.device), ctypes.byref(desc)), name)
     return PackedLayer(buf, desc, d, F)
 
 
@@ -334,7 +344,7 @@ __all__ = [
     "prox_choose_sparsity", "prox_cost_model", "prox_cost_model_bytes",
     "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",
-    "prox_launch_count",
+    "prox_launch_count", "prox_packed_bytes_fp8", "FORMAT_BF16", "FORMAT_FP8",
     "prox_k_for", "prox_pack_weights", "prox_packed_bytes", "prox_rmsnorm", "prox_sparse_ffn",
     "prox_sparse_ffn_noalloc",
     "prox_workspace", "prox_workspace_bytes", "prox_workspace_init",

@@ -48,9 +48,15 @@ int device_sms() {
 int check_packed(const prox_packed* w) {
     if (!w || !w->base) return PROX_ERR_INVALID_ARG;
     if (w->group != PROX_GROUP || !shape_ok(w->d_model, w->d_ff)) return PROX_ERR_INVALID_ARG;
+    if (w->format != PROX_FORMAT_BF16 && w->format != PROX_FORMAT_FP8) return PROX_ERR_INVALID_ARG;
     if (!aligned(w->base, kAlign)) return PROX_ERR_WORKSPACE;
-    if (w->bytes < packed_layout(w->d_model, w->d_ff).total) return PROX_ERR_WORKSPACE;
+    if (w->bytes < packed_layout(w->d_model, w->d_ff, w->format).total) return PROX_ERR_WORKSPACE;
     return PROX_OK;
+}
+
+// Stage 2 over FP8 rows runs in the single-token fused kernel only.
+bool fp8_stage2_ok(const prox_packed* w, int batch, int sms) {
+    return w->format != PROX_FORMAT_FP8 || (batch == 1 && fused_supported(w->d_model, w->d_ff, sms));
 }
 
 int check_ws(void* ws, size_t ws_bytes, int d, int F, int B, int sms, WsLayout& W) {
@@ -129,7 +135,7 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
              float* y, int32_t* idx_out, uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s,
              const Debug* dbg) {
     const int d = w->d_model, F = w->d_ff;
-    const PackedLayout L = packed_layout(d, F);
+    const PackedLayout L = packed_layout(d, F, w->format);
     const uint8_t* packed = static_cast<const uint8_t*>(w->base);
     const int k = k_rule(sparsity, F);
     const int k_in = k_rule(in_sparsity, d);
@@ -139,6 +145,7 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
     uint32_t* ubits = reinterpret_cast<uint32_t*>(ws + W.ubits);
     const bool tc = y && !dbg && use_tc(w, B, W, sms);
+    if (y && !fp8_stage2_ok(w, B, sms)) return PROX_ERR_UNSUPPORTED;
     if (B == 1 && !g_fused_sel && fused_supported(d, F, sms)) {
         // one token: the whole path in one persistent launch
         FusedCall c;
@@ -289,24 +296,45 @@ int prox_k_for(double sparsity, int n) {
     return k_rule(sparsity, n);
 }
 
-int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
-                      int d_model, int d_ff, int group, void* packed_dev, size_t packed_bytes,
-                      void* stream, prox_packed* out) {
+namespace {
+int pack_format(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                int d_model, int d_ff, int group, void* packed_dev, size_t packed_bytes,
+                void* stream, prox_packed* out, int format) {
     if (!w_gate || !w_up || !w_down || !packed_dev || !out) return PROX_ERR_INVALID_ARG;
     if (group != PROX_GROUP || !shape_ok(d_model, d_ff)) return PROX_ERR_INVALID_ARG;
     if (!aligned(w_gate, 16) || !aligned(w_up, 16) || !aligned(w_down, 16)) return PROX_ERR_INVALID_ARG;
     if (!aligned(packed_dev, kAlign)) return PROX_ERR_WORKSPACE;
-    const PackedLayout L = packed_layout(d_model, d_ff);
+    const PackedLayout L = packed_layout(d_model, d_ff, format);
     if (packed_bytes < L.total) return PROX_ERR_WORKSPACE;
     PROX_TRY(launch_pack(w_gate, w_up, w_down, d_model, d_ff, L, static_cast<uint8_t*>(packed_dev),
                          static_cast<cudaStream_t>(stream)));
     out->d_model = d_model;
     out->d_ff = d_ff;
     out->group = group;
-    out->reserved = 0;
+    out->format = format;
     out->base = packed_dev;
     out->bytes = packed_bytes;
     return PROX_OK;
+}
+}  // namespace
+
+int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                      int d_model, int d_ff, int group, void* packed_dev, size_t packed_bytes,
+                      void* stream, prox_packed* out) {
+    return pack_format(w_gate, w_up, w_down, d_model, d_ff, group, packed_dev, packed_bytes, stream,
+                       out, PROX_FORMAT_BF16);
+}
+
+int prox_pack_weights_fp8(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                          int d_model, int d_ff, int group, void* packed_dev, size_t packed_bytes,
+                          void* stream, prox_packed* out) {
+    return pack_format(w_gate, w_up, w_down, d_model, d_ff, group, packed_dev, packed_bytes, stream,
+                       out, PROX_FORMAT_FP8);
+}
+
+size_t prox_packed_bytes_fp8(int d_model, int d_ff, int group) {
+    if (group != PROX_GROUP || !shape_ok(d_model, d_ff)) return 0;
+    return packed_layout(d_model, d_ff, PROX_FORMAT_FP8).total;
 }
 
 int prox_build_mask(const prox_packed* w, const float* x, int batch, double sparsity,
@@ -334,8 +362,9 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
     if (sms <= 0) return PROX_ERR_CUDA;
     WsLayout W;
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    const PackedLayout L = packed_layout(w->d_model, w->d_ff);
+    const PackedLayout L = packed_layout(w->d_model, w->d_ff, w->format);
     const int d = w->d_model;
+    if (!fp8_stage2_ok(w, batch, sms)) return PROX_ERR_UNSUPPORTED;
     if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
         FusedCall c;
         c.x = x;
@@ -404,8 +433,9 @@ int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, vo
     if (sms <= 0) return PROX_ERR_CUDA;
     WsLayout W;
     PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    const PackedLayout L = packed_layout(w->d_model, w->d_ff);
+    const PackedLayout L = packed_layout(w->d_model, w->d_ff, w->format);
     const int d = w->d_model;
+    if (!fp8_stage2_ok(w, batch, sms)) return PROX_ERR_UNSUPPORTED;
     if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
         FusedCall c;
         c.x = x;
@@ -493,7 +523,8 @@ int prox_debug_fused_forward(const prox_packed* w, const float* x, double sparsi
     if (!x || !y || !sel_out) return PROX_ERR_INVALID_ARG;
     if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
-    if (k_rule(sparsity, w->d_ff) == w->d_ff || !stage2_select_supported(w->d_model, w->d_ff))
+    if (k_rule(sparsity, w->d_ff) == w->d_ff || !stage2_select_supported(w->d_model, w->d_ff) ||
+        w->format != PROX_FORMAT_BF16)
         return PROX_ERR_UNSUPPORTED;
     const int sms = device_sms();
     if (sms <= 0) return PROX_ERR_CUDA;

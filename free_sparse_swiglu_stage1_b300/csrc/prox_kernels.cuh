@@ -11,15 +11,18 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 
 // ------------------------------------------------------------------ packed layer layout
 struct PackedLayout {
-    size_t codes_off, scales_off, rows_off, total;
+    size_t codes_off, scales_off, rows_off, row_bytes, total;
+    int format;   // PROX_FORMAT_BF16: rows [F][3][d] bf16; PROX_FORMAT_FP8: [F][3 d + 16] bytes
 };
 
-inline PackedLayout packed_layout(int d, int F) {
+inline PackedLayout packed_layout(int d, int F, int format = PROX_FORMAT_BF16) {
     PackedLayout L;
+    L.format = format;
     L.codes_off = 0;
     L.scales_off = align_up(static_cast<size_t>(d) * F);
     L.rows_off = align_up(L.scales_off + static_cast<size_t>(d / 128) * F * 4);
-    L.total = align_up(L.rows_off + static_cast<size_t>(F) * 3 * d * 2);
+    L.row_bytes = format == PROX_FORMAT_FP8 ? static_cast<size_t>(3) * d + 16 : static_cast<size_t>(6) * d;
+    L.total = align_up(L.rows_off + static_cast<size_t>(F) * L.row_bytes);
     return L;
 }
 

@@ -49,6 +49,7 @@ extern "C" int prox_sparse_ffn_noalloc(const prox_packed* w, const float* x, int
     const int d = w->d_model, F = w->d_ff;
     if (w->group != PROX_GROUP || d < 128 || d % 128 != 0 || F < 32 || F % 32 != 0)
         return PROX_ERR_INVALID_ARG;
+    if (w->format != PROX_FORMAT_BF16) return PROX_ERR_UNSUPPORTED;   // bf16 rows only
     if (batch < 1 || batch > PROX_MAX_BATCH || k < 1 || k > F) return PROX_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y)) return PROX_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(w->base) % kAlign) != 0) return PROX_ERR_WORKSPACE;

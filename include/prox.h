@@ -49,12 +49,15 @@ extern "C" {
 #define PROX_ERR_UNSUPPORTED (-6)  /* valid request the library does not implement        */
 
 #define PROX_GROUP      128        /* proxy quantization group along d_model               */
+#define PROX_FORMAT_BF16  0        /* packed Stage-2 rows: the layer's bf16 weights        */
+#define PROX_FORMAT_FP8   1        /* packed Stage-2 rows: FP8 E4M3 with fp32 row scales   */
 #define PROX_MAX_BATCH  16         /* tokens per call                                      */
 #define PROX_ALIGN      256        /* required alignment of packed and workspace buffers   */
 
 /* Descriptor of one packed layer. A plain view of caller-owned device memory that
- * prox_pack_weights fills; copy it freely. Field meaning:
+ * prox_pack_weights (or prox_pack_weights_fp8) fills; copy it freely. Field meaning:
  *   d_model, d_ff, group  the layer shape and the proxy group (128);
+ *   format                PROX_FORMAT_BF16 or PROX_FORMAT_FP8 (how the Stage-2 rows are kept);
  *   base, bytes           the packed device buffer (PROX_ALIGN-aligned) and its size.
  * Packed layout inside base (offsets are multiples of PROX_ALIGN, in this order):
  *   codes  [d_model][d_ff] uint8: byte (i, j) holds the INT4 proxy codes of input i for
@@ -63,12 +66,15 @@ extern "C" {
  *   scales [d_model/128][d_ff] uint32: the fp16 group scales, W_gate's in the low half and
  *          W_up's in the high half;
  *   rows   [d_ff][3][d_model] bf16: for channel j the rows W_gate[j,:], W_up[j,:] and
- *          W_down[:,j] one after another (channel-major, one contiguous run per channel). */
+ *          W_down[:,j] one after another (channel-major, one contiguous run per channel).
+ *          With PROX_FORMAT_FP8 instead [d_ff][3 d_model + 16] bytes: per channel the same
+ *          three rows as FP8 E4M3 codes (one byte each), then the three rows' fp32 scales
+ *          and one fp32 zero; a weight is code * scale. */
 typedef struct prox_packed {
     int32_t d_model;
     int32_t d_ff;
     int32_t group;
-    int32_t reserved;
+    int32_t format;
     void*   base;
     size_t  bytes;
 } prox_packed;
@@ -112,6 +118,9 @@ int prox_choose_sparsity(const prox_cost_model* cost, int d_model, int d_ff, dou
 /* Bytes prox_pack_weights needs for one layer; 0 if the shape is invalid. */
 size_t prox_packed_bytes(int d_model, int d_ff, int group);
 
+/* Bytes prox_pack_weights_fp8 needs for one layer; 0 if the shape is invalid. */
+size_t prox_packed_bytes_fp8(int d_model, int d_ff, int group);
+
 /* Workspace bytes a call on this layer shape and batch needs on the CURRENT device (it
  * depends on the device's SM count); 0 if the shape is invalid. One workspace serves every
  * call on shapes no larger than the ones it was sized for. */
@@ -139,6 +148,21 @@ int prox_k_for(double sparsity, int n);
 int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                       int d_model, int d_ff, int group,
                       void* packed_dev, size_t packed_bytes, void* stream, prox_packed* out);
+
+/* prox_pack_weights with the Stage-2 rows kept as FP8 E4M3 instead of bf16 (technical
+ * summary, "Experimental Results", Compatibility: Prox is orthogonal to weight quantization
+ * such as FP8). The INT4 proxies are built from the same bf16 weights as in
+ * prox_pack_weights, so Stage 1 and the mask do not change; Stage 2 multiplies with the
+ * FP8 weights and reads half the bytes. Rule per row r (W_gate[j,:], W_up[j,:], W_down[:,j]):
+ * s = fp32(max |w|) / 448, code = e4m3(fp32(w) / s) rounded to nearest even and saturated
+ * at 448 (both divisions in IEEE binary32), code = 0 if s == 0. Arguments as for
+ * prox_pack_weights (packed_bytes >= prox_packed_bytes_fp8); out->format = PROX_FORMAT_FP8.
+ * Calls that run Stage 2 on such a layer (prox_sparse_ffn, prox_ffn_forward,
+ * prox_ffn_forward_host, prox_dense_ffn) accept one token per call and return
+ * PROX_ERR_UNSUPPORTED for a batch; prox_build_mask and prox_debug_stage1 accept any batch. */
+int prox_pack_weights_fp8(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
+                          int d_model, int d_ff, int group,
+                          void* packed_dev, size_t packed_bytes, void* stream, prox_packed* out);
 
 /* Stage 1 alone: input sparsity, INT4 proxy projections, salience |SiLU(g~) * u~| and the
  * top-k channel mask (technical summary, Stage 1 "Proxy Activation" and "Mask

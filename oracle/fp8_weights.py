@@ -12,8 +12,9 @@ rows being W_gate[j, :], W_up[j, :] and W_down[:, j] of channel j:
     s = fp32(max |w|) / 448      (binary32 divide)
     q = e4m3(fp32(w) / s)         (binary32 divide, round to nearest even, saturating at 448)
     q = 0 where s = 0
-and the dequantized weight is q * s (exact in fp64). Stage 2 over FP8 weights is
-stage2_exact over the dequantized matrices.
+and the dequantized weight is q * s (exact in fp64). A quotient that rounds to zero keeps
+its sign, as IEEE rounding does (a tiny negative weight has code 0x80, value -0). Stage 2
+over FP8 weights is stage2_exact over the dequantized matrices.
 Pinned in tests/test_fp8_oracle.py: the value set against the format's closed-form
 definition, the rounding against torch's float8_e4m3fn cast, saturation, and the row scale.
 """
@@ -43,7 +44,7 @@ def e4m3_bits(q) -> np.ndarray:
     """The 8-bit codes of E4M3 values (sign | exponent << 3 | mantissa)."""
     q = np.asarray(q, dtype=np.float64)
     a = np.abs(q)
-    sign = (np.signbit(q) & (a > 0)).astype(np.uint8) << 7
+    sign = np.signbit(q).astype(np.uint8) << 7   # a negative zero keeps its sign bit
     with np.errstate(divide="ignore"):
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     normal = e >= E4M3_MIN_EXP

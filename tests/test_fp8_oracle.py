@@ -47,6 +47,11 @@ def test_rounding_matches_torch_cast():
 def test_saturation_and_zero():
     got = F8.e4m3_round(np.array([448.0, 449.0, 470.0, 1e6, -1e9, 0.0, -0.0], np.float32))
     np.testing.assert_array_equal(got, [448, 448, 448, 448, -448, 0, 0])
+    # values that round to zero keep their sign, as torch's cast does
+    tiny = np.array([1e-4, -1e-4, 2.0 ** -11, -(2.0 ** -11), 0.0, -0.0], np.float32)
+    want = torch.from_numpy(tiny).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(F8.e4m3_bits(F8.e4m3_round(tiny)), want)
+    assert list(want) == [0, 0x80, 0, 0x80, 0, 0x80]
 
 
 def test_row_scale_rule():
