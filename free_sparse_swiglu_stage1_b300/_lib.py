@@ -33,7 +33,8 @@ class prox_cost_model(ctypes.Structure):
 class prox_packed(ctypes.Structure):
     _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("group", ctypes.c_int32), ("format", ctypes.c_int32),
-                ("base", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+                ("base", ctypes.c_void_p), ("bytes", ctypes.c_size_t),
+                ("proxy", ctypes.c_void_p)]
 
 
 _P = ctypes.POINTER(prox_packed)
@@ -66,6 +67,16 @@ SIGNATURES = {
     "prox_debug_union": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_fused_forward": (_i, [_P, _vp, _d, _d, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_wait_timeout": (_i, [_vp, _sz, ctypes.c_longlong, _vp]),
+    "prox_proxy_bytes": (_sz, [_i, _i, _i]),
+    "prox_rows_bytes": (_sz, [_i, _i, _i, _i]),
+    "prox_split_packed": (_i, [_P, _vp, _sz, _vp, _sz, _vp, _P]),
+    "prox_window_create": (_i, [_i, _i, _i, _i, ctypes.POINTER(_vp), _vp, _sz,
+                                ctypes.POINTER(_vp)]),
+    "prox_window_acquire": (_i, [_vp, _i, _P, _vp]),
+    "prox_window_release": (_i, [_vp, _i, _vp]),
+    "prox_window_stats": (_i, [_vp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "prox_window_destroy": (_i, [_vp]),
+    "prox_debug_window_plan": (_i, [_i, _i, _vp, _i, _vp, _vp, _i, ctypes.POINTER(_i)]),
 }
 
 _lib: ctypes.CDLL | None = None

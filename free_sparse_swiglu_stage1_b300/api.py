@@ -15,7 +15,8 @@ from . import _lib
 from ._lib import ProxError, prox_cost_model, prox_packed
 
 GROUP = 128
-MAX_BATCH = 16
+MAX_BATCH = 16      # tokens per tile (one pass of the batch kernels)
+MAX_TOKENS = 1024   # tokens per call; larger calls run tile by tile
 
 
 def _stream(stream, device) -> int:
@@ -141,6 +142,109 @@ def prox_pack_weights(w_gate: torch.Tensor, w_up: torch.Tensor, w_down: torch.Te
     _lib.check(getattr(_lib.lib(), name)(pg, pu, pd, d, F, group, buf.data_ptr(), n,
                                          _stream(stream, w_gate.device), ctypes.byref(desc)), name)
     return PackedLayer(buf, desc, d, F)
+
+
+def prox_proxy_bytes(d_model: int, d_ff: int, group: int = GROUP) -> int:
+    return int(_lib.lib().prox_proxy_bytes(d_model, d_ff, group))
+
+
+def prox_rows_bytes(d_model: int, d_ff: int, group: int = GROUP, fp8: bool = False) -> int:
+    return int(_lib.lib().prox_rows_bytes(d_model, d_ff, group, FORMAT_FP8 if fp8 else FORMAT_BF16))
+
+
+@dataclass
+class SplitLayer(PackedLayer):
+    """A packed layer split into device-resident rows (buffer) and its proxy (proxy_buffer:
+    pinned host memory, or device memory)."""
+    proxy_buffer: torch.Tensor | None = None
+
+
+def prox_split_packed(layer: PackedLayer, proxy_on_host: bool = True, stream=None) -> SplitLayer:
+    """Copies the layer's rows to a device buffer of their own and its proxy to pinned host
+    memory (or, with proxy_on_host=False, to a device buffer); waits for the copies, so the
+    full packed buffer may be dropped afterwards."""
+    d, F = layer.d_model, layer.d_ff
+    fp8 = layer.desc.format == FORMAT_FP8
+    rb, pb = prox_rows_bytes(d, F, fp8=fp8), prox_proxy_bytes(d, F)
+    dev = layer.buffer.device
+    rows = torch.empty(rb, dtype=torch.uint8, device=dev)
+    proxy = (torch.empty(pb, dtype=torch.uint8, pin_memory=True) if proxy_on_host
+             else torch.empty(pb, dtype=torch.uint8, device=dev))
+    desc = prox_packed()
+    st = _stream(stream, dev)
+    _lib.check(_lib.lib().prox_split_packed(layer.ref, rows.data_ptr(), rb, proxy.data_ptr(), pb, st,
+                                            ctypes.byref(desc)), "prox_split_packed")
+    torch.cuda.current_stream(dev).synchronize() if stream is None else stream.synchronize()
+    return SplitLayer(rows, desc, d, F, proxy)
+
+
+class ProxyWindow:
+    """A sliding window of n_slots device-resident proxies over a stack of split layers
+    (prox_window_*). Usage per layer visit: window.acquire(l) -> a descriptor whose proxy
+    points at the slot; run the layer's calls; window.release(l)."""
+
+    def __init__(self, layers: list[SplitLayer], n_slots: int, device=None):
+        if not layers:
+            raise ValueError("a window needs at least one layer")
+        d, F = layers[0].d_model, layers[0].d_ff
+        if any((l.d_model, l.d_ff) != (d, F) for l in layers):
+            raise ValueError("every layer of a window has one shape")
+        if any(l.proxy_buffer is None or l.proxy_buffer.is_cuda for l in layers):
+            raise ValueError("the layers' proxies must be in host memory")
+        self.layers = layers
+        self.device = torch.device(device) if device is not None else layers[0].buffer.device
+        pb = prox_proxy_bytes(d, F)
+        self.slots = torch.empty(n_slots * pb, dtype=torch.uint8, device=self.device)
+        ptrs = (ctypes.c_void_p * len(layers))(*[l.proxy_buffer.data_ptr() for l in layers])
+        self._handle = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            _lib.check(_lib.lib().prox_window_create(len(layers), n_slots, d, F, ptrs,
+                                                     self.slots.data_ptr(), self.slots.numel(),
+                                                     ctypes.byref(self._handle)),
+                       "prox_window_create")
+        self._descs = [prox_packed.from_buffer_copy(l.desc) for l in layers]
+
+    def acquire(self, layer: int, stream=None) -> PackedLayer:
+        desc = self._descs[layer]
+        _lib.check(_lib.lib().prox_window_acquire(self._handle, layer, ctypes.byref(desc),
+                                                  _stream(stream, self.device)),
+                   "prox_window_acquire")
+        src = self.layers[layer]
+        return PackedLayer(src.buffer, desc, src.d_model, src.d_ff)
+
+    def release(self, layer: int, stream=None) -> None:
+        _lib.check(_lib.lib().prox_window_release(self._handle, layer, _stream(stream, self.device)),
+                   "prox_window_release")
+
+    def stats(self) -> tuple[int, int]:
+        c, b = ctypes.c_uint64(), ctypes.c_uint64()
+        _lib.check(_lib.lib().prox_window_stats(self._handle, ctypes.byref(c), ctypes.byref(b)),
+                   "prox_window_stats")
+        return int(c.value), int(b.value)
+
+    def close(self) -> None:
+        if self._handle:
+            _lib.lib().prox_window_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def prox_debug_window_plan(n_layers: int, n_slots: int, ops: list[int], copy_cap: int = 4096):
+    """The window's slot policy on the host alone: (slot per op, [(op, slot, layer)] copies)."""
+    n = len(ops)
+    arr = (ctypes.c_int * max(n, 1))(*ops)
+    slots = (ctypes.c_int * max(n, 1))()
+    log = (ctypes.c_int * (3 * max(copy_cap, 1)))()
+    nc = ctypes.c_int()
+    _lib.check(_lib.lib().prox_debug_window_plan(n_layers, n_slots, arr, n, slots, log, copy_cap,
+                                                 ctypes.byref(nc)), "prox_debug_window_plan")
+    copies = [(log[3 * i], log[3 * i + 1], log[3 * i + 2]) for i in range(min(nc.value, copy_cap))]
+    return list(slots)[:n], copies, nc.value
 
 
 def _x(layer: PackedLayer, x: torch.Tensor) -> tuple[int, int]:
@@ -340,7 +444,8 @@ def prox_debug_wait_timeout(ws: Workspace, spin_cycles: int, stream=None) -> Non
 
 
 __all__ = [
-    "GROUP", "MAX_BATCH", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
+    "GROUP", "MAX_BATCH", "MAX_TOKENS", "ProxyWindow", "SplitLayer", "prox_proxy_bytes",
+    "prox_rows_bytes", "prox_split_packed", "prox_debug_window_plan", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
     "prox_choose_sparsity", "prox_cost_model", "prox_cost_model_bytes",
     "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",

@@ -50,7 +50,15 @@ int check_packed(const prox_packed* w) {
     if (w->group != PROX_GROUP || !shape_ok(w->d_model, w->d_ff)) return PROX_ERR_INVALID_ARG;
     if (w->format != PROX_FORMAT_BF16 && w->format != PROX_FORMAT_FP8) return PROX_ERR_INVALID_ARG;
     if (!aligned(w->base, kAlign)) return PROX_ERR_WORKSPACE;
-    if (w->bytes < packed_layout(w->d_model, w->d_ff, w->format).total) return PROX_ERR_WORKSPACE;
+    if (w->proxy) {
+        if (!aligned(w->proxy, kAlign)) return PROX_ERR_WORKSPACE;
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, w->proxy) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            return PROX_ERR_INVALID_ARG;   // a split layer's proxy must be in device memory
+        }
+    }
+    if (w->bytes < packed_layout_of(w).total) return PROX_ERR_WORKSPACE;
     return PROX_OK;
 }
 
@@ -135,7 +143,7 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
              float* y, int32_t* idx_out, uint8_t* ws, const WsLayout& W, int sms, cudaStream_t s,
              const Debug* dbg) {
     const int d = w->d_model, F = w->d_ff;
-    const PackedLayout L = packed_layout(d, F, w->format);
+    const PackedLayout L = packed_layout_of(w);
     const uint8_t* packed = static_cast<const uint8_t*>(w->base);
     const int k = k_rule(sparsity, F);
     const int k_in = k_rule(in_sparsity, d);
@@ -214,6 +222,22 @@ int run_path(const prox_packed* w, const float* x, int B, double sparsity, doubl
     return PROX_OK;
 }
 
+// Tokens of one tile: calls above PROX_MAX_BATCH tokens run tile by tile, every tile exactly
+// as a call of its own (each token keeps its own inputs and mask, so tiling changes nothing
+// but the number of passes over the weights).
+inline int tile_batch(int batch) { return batch < PROX_MAX_BATCH ? batch : PROX_MAX_BATCH; }
+
+template <class Fn>
+int for_token_tiles(int batch, Fn&& fn) {
+    for (int t0 = 0; t0 < batch; t0 += PROX_MAX_BATCH) {
+        const int nb = batch - t0 < PROX_MAX_BATCH ? batch - t0 : PROX_MAX_BATCH;
+        PROX_TRY(fn(t0, nb));
+    }
+    return PROX_OK;
+}
+
+bool tokens_ok(int batch) { return batch >= 1 && batch <= PROX_MAX_TOKENS; }
+
 }  // namespace
 
 extern "C" {
@@ -224,10 +248,10 @@ size_t prox_packed_bytes(int d_model, int d_ff, int group) {
 }
 
 size_t prox_workspace_bytes(int d_model, int d_ff, int batch) {
-    if (!shape_ok(d_model, d_ff) || batch < 1 || batch > PROX_MAX_BATCH) return 0;
+    if (!shape_ok(d_model, d_ff) || !tokens_ok(batch)) return 0;
     const int sms = device_sms();
     if (sms <= 0) return 0;
-    return ws_layout(d_model, d_ff, batch, sms).total;
+    return ws_layout(d_model, d_ff, tile_batch(batch), sms).total;
 }
 
 int prox_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -314,6 +338,7 @@ int pack_format(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_
     out->format = format;
     out->base = packed_dev;
     out->bytes = packed_bytes;
+    out->proxy = nullptr;
     return PROX_OK;
 }
 }  // namespace
@@ -341,30 +366,28 @@ int prox_build_mask(const prox_packed* w, const float* x, int batch, double spar
                     double input_sparsity, int32_t* idx_out, void* ws, size_t ws_bytes,
                     void* stream) {
     PROX_TRY(check_packed(w));
-    if (!x || !idx_out || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
+    if (!x || !idx_out || !tokens_ok(batch)) return PROX_ERR_INVALID_ARG;
     if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
     if (!aligned(x, 16)) return PROX_ERR_INVALID_ARG;
     const int sms = device_sms();
     if (sms <= 0) return PROX_ERR_CUDA;
     WsLayout W;
-    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    return run_path(w, x, batch, sparsity, input_sparsity, nullptr, idx_out,
-                    static_cast<uint8_t*>(ws), W, sms, static_cast<cudaStream_t>(stream), nullptr);
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, tile_batch(batch), sms, W));
+    const int d = w->d_model, F = w->d_ff, k = k_rule(sparsity, F);
+    return for_token_tiles(batch, [&](int t0, int nb) {
+        return run_path(w, x + static_cast<size_t>(t0) * d, nb, sparsity, input_sparsity, nullptr,
+                        idx_out + static_cast<size_t>(t0) * k, static_cast<uint8_t*>(ws),
+                        ws_layout(d, F, nb, sms), sms, static_cast<cudaStream_t>(stream), nullptr);
+    });
 }
 
-int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx, int k,
-                    float* y, void* ws, size_t ws_bytes, void* stream) {
-    PROX_TRY(check_packed(w));
-    if (!x || !idx || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
-    if (k < 1 || k > w->d_ff) return PROX_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
-    const int sms = device_sms();
-    if (sms <= 0) return PROX_ERR_CUDA;
-    WsLayout W;
-    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    const PackedLayout L = packed_layout(w->d_model, w->d_ff, w->format);
+namespace {
+
+// Stage 2 of one tile of at most PROX_MAX_BATCH tokens over a given mask.
+int sparse_ffn_tile(const prox_packed* w, const float* x, int batch, const int32_t* idx, int k,
+                    float* y, void* ws, const WsLayout& W, int sms, void* stream) {
+    const PackedLayout L = packed_layout_of(w);
     const int d = w->d_model;
-    if (!fp8_stage2_ok(w, batch, sms)) return PROX_ERR_UNSUPPORTED;
     if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
         FusedCall c;
         c.x = x;
@@ -388,54 +411,11 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
     return PROX_OK;
 }
 
-int prox_ffn_forward(const prox_packed* w, const float* x, int batch, double sparsity,
-                     double input_sparsity, float* y, int32_t* idx_out, void* ws, size_t ws_bytes,
-                     void* stream) {
-    PROX_TRY(check_packed(w));
-    if (!x || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
-    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
-    const int sms = device_sms();
-    if (sms <= 0) return PROX_ERR_CUDA;
-    WsLayout W;
-    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    return run_path(w, x, batch, sparsity, input_sparsity, y, idx_out, static_cast<uint8_t*>(ws), W,
-                    sms, static_cast<cudaStream_t>(stream), nullptr);
-}
-
-int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch, double sparsity,
-                          double input_sparsity, float* y_host, void* ws, size_t ws_bytes,
-                          void* stream) {
-    PROX_TRY(check_packed(w));
-    if (!x_host || !y_host || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
-    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
-    const int sms = device_sms();
-    if (sms <= 0) return PROX_ERR_CUDA;
-    WsLayout W;
-    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* wsb = static_cast<uint8_t*>(ws);
-    float* xd = reinterpret_cast<float*>(wsb + W.xbuf);
-    float* yd = reinterpret_cast<float*>(wsb + W.ybuf);
-    const size_t bytes = static_cast<size_t>(batch) * w->d_model * sizeof(float);
-    PROX_TRY(cuda_ok(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s), "copying x to the device"));
-    PROX_TRY(run_path(w, xd, batch, sparsity, input_sparsity, yd, nullptr, wsb, W, sms, s, nullptr));
-    PROX_TRY(cuda_ok(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s), "copying y to the host"));
-    return cuda_ok(cudaStreamSynchronize(s), "waiting for the stream");
-}
-
-int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, void* ws,
-                   size_t ws_bytes, void* stream) {
-    PROX_TRY(check_packed(w));
-    if (!x || !y || batch < 1 || batch > PROX_MAX_BATCH) return PROX_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
-    const int sms = device_sms();
-    if (sms <= 0) return PROX_ERR_CUDA;
-    WsLayout W;
-    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, batch, sms, W));
-    const PackedLayout L = packed_layout(w->d_model, w->d_ff, w->format);
+// Stage 2 over every channel for one tile of at most PROX_MAX_BATCH tokens.
+int dense_ffn_tile(const prox_packed* w, const float* x, int batch, float* y, void* ws,
+                   const WsLayout& W, int sms, void* stream) {
+    const PackedLayout L = packed_layout_of(w);
     const int d = w->d_model;
-    if (!fp8_stage2_ok(w, batch, sms)) return PROX_ERR_UNSUPPORTED;
     if (batch == 1 && fused_supported(d, w->d_ff, sms)) {
         FusedCall c;
         c.x = x;
@@ -455,6 +435,94 @@ int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, vo
                                  static_cast<cudaStream_t>(stream)));
     }
     return PROX_OK;
+}
+
+}  // namespace
+
+int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32_t* idx, int k,
+                    float* y, void* ws, size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !idx || !y || !tokens_ok(batch)) return PROX_ERR_INVALID_ARG;
+    if (k < 1 || k > w->d_ff) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, tile_batch(batch), sms, W));
+    if (!fp8_stage2_ok(w, tile_batch(batch), sms)) return PROX_ERR_UNSUPPORTED;
+    const int d = w->d_model, F = w->d_ff;
+    return for_token_tiles(batch, [&](int t0, int nb) {
+        return sparse_ffn_tile(w, x + static_cast<size_t>(t0) * d, nb,
+                               idx + static_cast<size_t>(t0) * k, k, y + static_cast<size_t>(t0) * d,
+                               ws, ws_layout(d, F, nb, sms), sms, stream);
+    });
+}
+
+int prox_ffn_forward(const prox_packed* w, const float* x, int batch, double sparsity,
+                     double input_sparsity, float* y, int32_t* idx_out, void* ws, size_t ws_bytes,
+                     void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !y || !tokens_ok(batch)) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, tile_batch(batch), sms, W));
+    const int d = w->d_model, F = w->d_ff, k = k_rule(sparsity, F);
+    return for_token_tiles(batch, [&](int t0, int nb) {
+        return run_path(w, x + static_cast<size_t>(t0) * d, nb, sparsity, input_sparsity,
+                        y + static_cast<size_t>(t0) * d,
+                        idx_out ? idx_out + static_cast<size_t>(t0) * k : nullptr,
+                        static_cast<uint8_t*>(ws), ws_layout(d, F, nb, sms), sms,
+                        static_cast<cudaStream_t>(stream), nullptr);
+    });
+}
+
+int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch, double sparsity,
+                          double input_sparsity, float* y_host, void* ws, size_t ws_bytes,
+                          void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x_host || !y_host || !tokens_ok(batch)) return PROX_ERR_INVALID_ARG;
+    if (!sparsity_ok(sparsity) || !sparsity_ok(input_sparsity)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, tile_batch(batch), sms, W));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const int d = w->d_model, F = w->d_ff;
+    PROX_TRY(for_token_tiles(batch, [&](int t0, int nb) {
+        // the tile's x and y go through the workspace's own buffers
+        const WsLayout Wt = ws_layout(d, F, nb, sms);
+        float* xd = reinterpret_cast<float*>(wsb + Wt.xbuf);
+        float* yd = reinterpret_cast<float*>(wsb + Wt.ybuf);
+        const size_t off = static_cast<size_t>(t0) * d;
+        const size_t bytes = static_cast<size_t>(nb) * d * sizeof(float);
+        PROX_TRY(cuda_ok(cudaMemcpyAsync(xd, x_host + off, bytes, cudaMemcpyHostToDevice, s),
+                         "copying x to the device"));
+        PROX_TRY(run_path(w, xd, nb, sparsity, input_sparsity, yd, nullptr, wsb, Wt, sms, s, nullptr));
+        return cuda_ok(cudaMemcpyAsync(y_host + off, yd, bytes, cudaMemcpyDeviceToHost, s),
+                       "copying y to the host");
+    }));
+    return cuda_ok(cudaStreamSynchronize(s), "waiting for the stream");
+}
+
+int prox_dense_ffn(const prox_packed* w, const float* x, int batch, float* y, void* ws,
+                   size_t ws_bytes, void* stream) {
+    PROX_TRY(check_packed(w));
+    if (!x || !y || !tokens_ok(batch)) return PROX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16)) return PROX_ERR_INVALID_ARG;
+    const int sms = device_sms();
+    if (sms <= 0) return PROX_ERR_CUDA;
+    WsLayout W;
+    PROX_TRY(check_ws(ws, ws_bytes, w->d_model, w->d_ff, tile_batch(batch), sms, W));
+    if (!fp8_stage2_ok(w, tile_batch(batch), sms)) return PROX_ERR_UNSUPPORTED;
+    const int d = w->d_model, F = w->d_ff;
+    return for_token_tiles(batch, [&](int t0, int nb) {
+        return dense_ffn_tile(w, x + static_cast<size_t>(t0) * d, nb, y + static_cast<size_t>(t0) * d,
+                              ws, ws_layout(d, F, nb, sms), sms, stream);
+    });
 }
 
 int prox_rmsnorm(const float* y, float* x_out, int batch, int d_model, float eps, void* stream) {

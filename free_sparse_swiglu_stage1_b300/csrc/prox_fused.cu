@@ -97,9 +97,9 @@ int launch_fused(const uint8_t* packed, const PackedLayout& L, int d, int F, con
     if (sms > W.P) return PROX_ERR_WORKSPACE;   // the partial outputs need one row per block
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), sh.smem) != PROX_OK) return PROX_ERR_CUDA;
     FusedParams p{};
-    p.codes = packed + L.codes_off;
-    p.scales = reinterpret_cast<const uint32_t*>(packed + L.scales_off);
-    p.rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
+    p.codes = L.codes(packed);
+    p.scales = L.scales(packed);
+    p.rows = reinterpret_cast<const uint16_t*>(L.rows(packed));
     p.row_bytes = L.row_bytes;
     p.x = c.x;
     p.d = d;

@@ -10,9 +10,19 @@ constexpr size_t kAlign = PROX_ALIGN;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ packed layer layout
+// One buffer holds codes, scales and rows at these offsets; a split layer keeps the proxy
+// (codes and scales, proxy_bytes) in a buffer of its own and only the rows (from offset 0) in
+// the packed buffer. Kernels get their operands through codes(), scales() and rows().
 struct PackedLayout {
-    size_t codes_off, scales_off, rows_off, row_bytes, total;
+    size_t codes_off, scales_off, rows_off, row_bytes, proxy_bytes, total;
     int format;   // PROX_FORMAT_BF16: rows [F][3][d] bf16; PROX_FORMAT_FP8: [F][3 d + 16] bytes
+    const uint8_t* proxy = nullptr;   // split layer: the proxy's own buffer
+
+    const uint8_t* codes(const uint8_t* packed) const { return (proxy ? proxy : packed) + codes_off; }
+    const uint32_t* scales(const uint8_t* packed) const {
+        return reinterpret_cast<const uint32_t*>((proxy ? proxy : packed) + scales_off);
+    }
+    const uint8_t* rows(const uint8_t* packed) const { return packed + rows_off; }
 };
 
 inline PackedLayout packed_layout(int d, int F, int format = PROX_FORMAT_BF16) {
@@ -20,9 +30,21 @@ inline PackedLayout packed_layout(int d, int F, int format = PROX_FORMAT_BF16) {
     L.format = format;
     L.codes_off = 0;
     L.scales_off = align_up(static_cast<size_t>(d) * F);
-    L.rows_off = align_up(L.scales_off + static_cast<size_t>(d / 128) * F * 4);
+    L.proxy_bytes = align_up(L.scales_off + static_cast<size_t>(d / 128) * F * 4);
+    L.rows_off = L.proxy_bytes;
     L.row_bytes = format == PROX_FORMAT_FP8 ? static_cast<size_t>(3) * d + 16 : static_cast<size_t>(6) * d;
     L.total = align_up(L.rows_off + static_cast<size_t>(F) * L.row_bytes);
+    return L;
+}
+
+// The layout of a descriptor: `total` is what its packed buffer must hold.
+inline PackedLayout packed_layout_of(const prox_packed* w) {
+    PackedLayout L = packed_layout(w->d_model, w->d_ff, w->format);
+    if (w->proxy) {
+        L.proxy = static_cast<const uint8_t*>(w->proxy);
+        L.rows_off = 0;
+        L.total = align_up(static_cast<size_t>(w->d_ff) * L.row_bytes);
+    }
     return L;
 }
 

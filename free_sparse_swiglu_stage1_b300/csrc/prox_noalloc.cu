@@ -53,7 +53,8 @@ extern "C" int prox_sparse_ffn_noalloc(const prox_packed* w, const float* x, int
     if (batch < 1 || batch > PROX_MAX_BATCH || k < 1 || k > F) return PROX_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y)) return PROX_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(w->base) % kAlign) != 0) return PROX_ERR_WORKSPACE;
-    const PackedLayout L = packed_layout(d, F);
+    if (w->proxy && (reinterpret_cast<uintptr_t>(w->proxy) % kAlign) != 0) return PROX_ERR_WORKSPACE;
+    const PackedLayout L = packed_layout_of(w);   // Stage 2 reads the rows only
     if (w->bytes < L.total) return PROX_ERR_WORKSPACE;
 
     int dev = 0, sms = 0;

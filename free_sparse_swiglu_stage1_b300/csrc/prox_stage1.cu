@@ -532,7 +532,7 @@ static int launch_stage1_t(const uint8_t* packed, const PackedLayout& L, int d, 
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     const cudaError_t err = cudaLaunchKernelEx(
-        &cfg, fn, packed + L.codes_off, reinterpret_cast<const uint32_t*>(packed + L.scales_off), d, F,
+        &cfg, fn, L.codes(packed), L.scales(packed), d, F,
         static_cast<const int*>(reinterpret_cast<const int*>(ws + W.grows)),
         static_cast<const int*>(reinterpret_cast<const int*>(ws + W.gq)),
         static_cast<const int8_t*>(reinterpret_cast<const int8_t*>(ws + W.gqx)),

@@ -325,7 +325,7 @@ int launch_stage1_tc(const uint8_t* packed, const PackedLayout& L, int d, int F,
     const int G = d / 128;
     const uint16_t* qxh = reinterpret_cast<const uint16_t*>(ws + W.qxh);
     CUtensorMap tm_codes, tm_qx;
-    if (encode_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, packed + L.codes_off, F, d, F, 128, 64,
+    if (encode_map_2d(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.codes(packed), F, d, F, 128, 64,
                       CU_TENSOR_MAP_SWIZZLE_NONE) != PROX_OK)
         return PROX_ERR_CUDA;
     if (encode_map_2d(&tm_qx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qxh, d, kTokens,
@@ -335,7 +335,7 @@ int launch_stage1_tc(const uint8_t* packed, const PackedLayout& L, int d, int F,
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(stage1_tc_kernel), smem) != PROX_OK)
         return PROX_ERR_CUDA;
     return launch_pdl(stage1_tc_kernel, dim3(sms), dim3(kThreads), smem, s, tm_codes, tm_qx,
-                      reinterpret_cast<const uint32_t*>(packed + L.scales_off),
+                      L.scales(packed),
                       reinterpret_cast<const float*>(ws + W.sx), d, F, B, sigma,
                       reinterpret_cast<int*>(ws + W.ghist), dbg_gate, dbg_up, kDefaultSpinCycles,
                       &reinterpret_cast<Control*>(ws + W.control)->status);

@@ -570,7 +570,7 @@ int launch_stage2(const uint8_t* packed, const PackedLayout& L, int d, int F, co
                   int nb, const int32_t* list, const uint32_t* lbits, const int* count_dev,
                   int count_host, float* y_tile, uint8_t* ws, const WsLayout& W, int sms,
                   cudaStream_t s) {
-    const uint16_t* rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
+    const uint16_t* rows = reinterpret_cast<const uint16_t*>(L.rows(packed));
     float* ypart = reinterpret_cast<float*>(ws + W.ypart);
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
     const int TB = nb <= 1 ? 1 : (nb <= 2 ? 2 : 4);
@@ -605,7 +605,7 @@ int launch_stage2_select(const uint8_t* packed, const PackedLayout& L, int d, in
                          int32_t* dbg_sel, uint8_t* ws, const WsLayout& W, int sms,
                          cudaStream_t s) {
     if (!stage2_select_supported(d, F)) return PROX_ERR_UNSUPPORTED;
-    const uint16_t* rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
+    const uint16_t* rows = reinterpret_cast<const uint16_t*>(L.rows(packed));
     float* ypart = reinterpret_cast<float*>(ws + W.ypart);
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
     const S2Shape sh = stage2_shape(d, 1);

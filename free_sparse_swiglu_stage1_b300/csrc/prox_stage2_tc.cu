@@ -473,7 +473,7 @@ int launch_stage2_tc(const uint8_t* packed, const PackedLayout& L, int d, int F,
     uint16_t* xhl = reinterpret_cast<uint16_t*>(ws + W.xhl);
     float* ypart = reinterpret_cast<float*>(ws + W.ypart);
     int* status = &reinterpret_cast<Control*>(ws + W.control)->status;
-    const uint16_t* rows = reinterpret_cast<const uint16_t*>(packed + L.rows_off);
+    const uint16_t* rows = reinterpret_cast<const uint16_t*>(L.rows(packed));
     // tile copies: a block's window of at most ceil(F / P) channels in nmt tiles of BH rows
     const int rmax = (F + P - 1) / P;
     const int nmt = (rmax + 127) / 128;

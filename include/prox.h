@@ -20,7 +20,14 @@
  *    a status word inside the workspace and reported by prox_get_status.
  *  - Layouts are row-major. bf16 is passed as uint16_t bit patterns.
  *  - Shapes: d_model a multiple of 128 in [128, 16384]; d_ff a multiple of 32 in
- *    [32, 53248]; batch in [1, PROX_MAX_BATCH]. Inputs must be finite.
+ *    [32, 53248]; batch in [1, PROX_MAX_TOKENS] (prox_debug_* and prox_sparse_ffn_noalloc:
+ *    [1, PROX_MAX_BATCH]). Inputs must be finite.
+ *  - Large batches: the pages leave large-batch serving open (technical summary,
+ *    "Significance and Claims", limitations). A call with more than PROX_MAX_BATCH tokens
+ *    runs as consecutive tiles of PROX_MAX_BATCH tokens (the last one ragged), each tile
+ *    exactly as a call of its own; every token still gets its own input set and mask, so the
+ *    result is the same as tile-sized calls. The workspace of such a call is that of one
+ *    full tile (prox_workspace_bytes returns the same size for any batch >= PROX_MAX_BATCH).
  *  - Sparsities are fractions in [0, 1). The kept counts are
  *        k    = clamp(floor((1 - sparsity) * d_ff + 0.5), 1, d_ff)
  *        k_in = clamp(floor((1 - input_sparsity) * d_model + 0.5), 1, d_model)
@@ -51,7 +58,8 @@ extern "C" {
 #define PROX_GROUP      128        /* proxy quantization group along d_model               */
 #define PROX_FORMAT_BF16  0        /* packed Stage-2 rows: the layer's bf16 weights        */
 #define PROX_FORMAT_FP8   1        /* packed Stage-2 rows: FP8 E4M3 with fp32 row scales   */
-#define PROX_MAX_BATCH  16         /* tokens per call                                      */
+#define PROX_MAX_BATCH  16         /* tokens per tile (one pass of the batch kernels)      */
+#define PROX_MAX_TOKENS 1024       /* tokens per call; larger calls run tile by tile       */
 #define PROX_ALIGN      256        /* required alignment of packed and workspace buffers   */
 
 /* Descriptor of one packed layer. A plain view of caller-owned device memory that
@@ -69,7 +77,12 @@ extern "C" {
  *          W_down[:,j] one after another (channel-major, one contiguous run per channel).
  *          With PROX_FORMAT_FP8 instead [d_ff][3 d_model + 16] bytes: per channel the same
  *          three rows as FP8 E4M3 codes (one byte each), then the three rows' fp32 scales
- *          and one fp32 zero; a weight is code * scale. */
+ *          and one fp32 zero; a weight is code * scale.
+ *   proxy  NULL for the layout above. Otherwise a split layer (prox_split_packed): the
+ *          proxy -- codes, then scales at the same offsets as above, prox_proxy_bytes
+ *          bytes -- lives at `proxy` (device memory, PROX_ALIGN-aligned) and base holds only
+ *          the rows, from offset 0 (prox_rows_bytes bytes). Compute calls check that proxy
+ *          is device memory and return PROX_ERR_INVALID_ARG if it is not. */
 typedef struct prox_packed {
     int32_t d_model;
     int32_t d_ff;
@@ -77,6 +90,7 @@ typedef struct prox_packed {
     int32_t format;
     void*   base;
     size_t  bytes;
+    void*   proxy;
 } prox_packed;
 
 /* Cost model of one layer for prox_choose_sparsity: per token, the sparse path costs
@@ -123,7 +137,8 @@ size_t prox_packed_bytes_fp8(int d_model, int d_ff, int group);
 
 /* Workspace bytes a call on this layer shape and batch needs on the CURRENT device (it
  * depends on the device's SM count); 0 if the shape is invalid. One workspace serves every
- * call on shapes no larger than the ones it was sized for. */
+ * call on shapes no larger than the ones it was sized for. A batch above PROX_MAX_BATCH
+ * needs the workspace of PROX_MAX_BATCH tokens. */
 size_t prox_workspace_bytes(int d_model, int d_ff, int batch);
 
 /* Clears the workspace's status word and its self-resetting counters. Call once after
@@ -263,6 +278,70 @@ const char* prox_last_cuda_error(void);
  * recorded (graph replays do not call the library). Memory copies and memsets are not kernel
  * launches of the library and are not counted. */
 uint64_t prox_launch_count(void);
+
+/* ---- Proxy-memory reduction: a sliding window of device-resident proxies over a layer stack.
+ * The pages name sliding-window schemes as the way to cut the ~12% memory the INT4 proxies
+ * add (technical summary, "Significance and Claims") and describe none. Reading used here:
+ * a decode step visits layers 0, 1, ..., L-1 in order (then 0 again for the next token).
+ * Every layer's proxy (the codes and scales Stage 1 reads) lives in pinned host memory and
+ * only S slots of proxies live in device memory. Acquiring layer l guarantees that l and the
+ * next S-1 layers (cyclically) are resident or being copied; releasing l lets the layer
+ * l+S take its slot. Copies run on the window's own stream, ordered by events after the
+ * compute that last read a slot and before the compute that reads it. Device memory for
+ * proxies drops from L * prox_proxy_bytes to S * prox_proxy_bytes; the price is the
+ * host-to-device traffic of one proxy per layer visit whenever S < L. */
+
+/* Bytes of one layer's proxy (codes and scales) and of its Stage-2 rows alone; 0 for an
+ * invalid shape or format. */
+size_t prox_proxy_bytes(int d_model, int d_ff, int group);
+size_t prox_rows_bytes(int d_model, int d_ff, int group, int format);
+
+/* Splits a packed layer (proxy == NULL) into its rows and its proxy: copies the rows to
+ * rows_dev (device, PROX_ALIGN-aligned, >= prox_rows_bytes) and the proxy to proxy_out (device
+ * or pinned host memory, PROX_ALIGN-aligned, >= prox_proxy_bytes), both enqueued on `stream`.
+ * `out` becomes the split descriptor {base = rows_dev, proxy = proxy_out}; it is usable by
+ * compute calls while proxy points at device memory holding this layer's proxy (the window
+ * sets it on every acquire). The full buffer may be freed once the copies have finished. */
+int prox_split_packed(const prox_packed* full, void* rows_dev, size_t rows_bytes,
+                      void* proxy_out, size_t proxy_bytes, void* stream, prox_packed* out);
+
+typedef struct prox_window prox_window;   /* opaque; one per layer stack */
+
+/* Creates a window of n_slots device slots over n_layers layers of one shape (group 128).
+ *   host_proxies [n_layers]: each layer's proxy as written by prox_split_packed, in pinned
+ *       host memory (pageable memory works but the copies then do not overlap compute);
+ *   slots_dev: device memory, PROX_ALIGN-aligned, >= n_slots * prox_proxy_bytes bytes.
+ * All three stay caller-owned and must outlive the window. The window creates one CUDA
+ * stream and 2 * n_slots events on the current device (freed by prox_window_destroy); it
+ * allocates no device memory. Not thread-safe: one window is driven from one host thread. */
+int prox_window_create(int n_layers, int n_slots, int d_model, int d_ff,
+                       const void* const* host_proxies, void* slots_dev, size_t slots_bytes,
+                       prox_window** out);
+
+/* Makes layer `layer`'s proxy available to work enqueued on `stream` after this call, and
+ * points desc->proxy (a split descriptor of that layer) at its slot. Issues the copies the
+ * window needs (this layer if it is not resident, then the following layers into free
+ * slots). PROX_ERR_UNSUPPORTED if every slot is held by an acquired, unreleased layer. */
+int prox_window_acquire(prox_window* w, int layer, prox_packed* desc, void* stream);
+
+/* Ends layer `layer`'s use of its slot: work enqueued on `stream` so far is its last reader.
+ * The slot is then refilled (after that work) with the next layer that enters the window.
+ * PROX_ERR_INVALID_ARG if the layer is not acquired. */
+int prox_window_release(prox_window* w, int layer, void* stream);
+
+/* Host-to-device copies the window has issued, and their bytes. */
+int prox_window_stats(const prox_window* w, uint64_t* copies, uint64_t* bytes);
+
+/* Waits for the window's copies, then frees its stream and events. */
+int prox_window_destroy(prox_window* w);
+
+/* Test hook: runs the window's slot policy on the host alone (no CUDA call). ops[i] >= 0
+ * acquires layer ops[i], ops[i] < 0 releases layer -1 - ops[i]. slot_out[i]: the slot the
+ * op used (-1: acquire found every slot in use, or release of a layer not acquired).
+ * copy_log [copy_cap][3]: (op index, slot, layer) of every copy in issue order; n_copies:
+ * how many copies were issued (may exceed copy_cap; only copy_cap are logged). */
+int prox_debug_window_plan(int n_layers, int n_slots, const int* ops, int n_ops, int* slot_out,
+                           int* copy_log, int copy_cap, int* n_copies);
 
 /* Test hook: the same input-selection and Stage-1 kernels as prox_build_mask, also storing
  * the exact integer intermediates (technical summary, Stage 1 "Proxy Activation").

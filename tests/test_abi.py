@@ -65,7 +65,7 @@ def test_forward_rejects_bad_arguments_before_launch(L):
     assert fwd(None, FAKE, 1, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
     assert fwd(ref, None, 1, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
     assert fwd(ref, FAKE, 0, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
-    assert fwd(ref, FAKE, 17, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
+    assert fwd(ref, FAKE, 1025, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
     assert fwd(ref, FAKE, 1, 1.0, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
     assert fwd(ref, FAKE, 1, 0.5, -0.2, FAKE, None, FAKE, 1 << 30, None) == E_ARG
     assert fwd(ref, FAKE + 4, 1, 0.5, 0.5, FAKE, None, FAKE, 1 << 30, None) == E_ARG
