@@ -123,7 +123,6 @@ int launch_fused(const uint8_t* packed, const PackedLayout& L, int d, int F, con
     p.write_idx = c.write_idx ? 1 : 0;
     // the code array must fit L2 several times over (126 MB on B300) to stay there
     p.prefetch_codes = 0;   // measured slower on the 4096 x 14336 layer: it delays the x loads
-    p.bulk_sigma = sh.bulk_sigma ? 1 : 0;
     p.dbg_qx = c.dbg_qx;
     p.dbg_sx = c.dbg_sx;
     p.dbg_gate = c.dbg_gate;

@@ -19,7 +19,6 @@ constexpr int kTileUnit = 8;     // Stage-1 tiles are whole units of 8 chunks of
 constexpr int kTopkKeysOff = 2 * 2048 * 4;   // the layer's salience keys, after two histograms
 constexpr int kCandCap = 4096;               // boundary-bin candidates ranked on their own
 constexpr int kTopkBar = 16;                 // mbarrier of the top-k's copies (ring: 0..15)
-constexpr int kCandDirect = 256;             // up to this many: ranked by direct counting
 
 struct FusedParams {
     const uint8_t* codes;
@@ -39,7 +38,6 @@ struct FusedParams {
     int region_bytes, nstage_log2, NG, WPG, CPT;
     int write_idx;   // also store the mask into idx (the caller asked for it)
     int prefetch_codes;   // bring the whole proxy code array into L2 at the start
-    int bulk_sigma;       // the top-k loads the salience by one bulk copy (staging room)
     int8_t* dbg_qx;
     float* dbg_sx;
     int32_t* dbg_gate;
@@ -399,6 +397,242 @@ __device__ void salience(const FusedParams& p, int c0, int nch, const int* s_A, 
     }
 }
 
+// ------------------------------------------------------------------ 4. top-k
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Run by one whole warp: over the nbins (<= 256) bins of h taken from the highest down, the
+// bin holding the remaining-th key (1 <= remaining <= the bins' total). sel[0] = the bin,
+// sel[1] = keys in higher bins, sel[2] = the bin's count.
+__device__ __forceinline__ void warp_find_digit(const int* h, int nbins, int remaining, int* sel) {
+    const int lane = threadIdx.x & 31;
+    int c[8], local = 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int r = lane * 8 + m;   // rank of the bin from the top
+        c[m] = r < nbins ? h[nbins - 1 - r] : 0;
+        local += c[m];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+    if (run < remaining && incl >= remaining) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            if (run < remaining && run + c[m] >= remaining) {
+                sel[0] = nbins - 1 - (lane * 8 + m);
+                sel[1] = run;
+                sel[2] = c[m];
+            }
+            run += c[m];
+        }
+    }
+}
+
+// Among the keys of a[0, n) whose bits 31..20 equal b1, taken in index order, marks the rem
+// largest in the channel bitmap wbits (equal keys go to the lower index; ch[i] is a[i]'s
+// channel, or i itself if ch is null). With cnt, a is a list of segments of `seg` slots and
+// only the first cnt[w] slots of segment w hold keys. Radix passes of 8, 8 and 4 bits over bits 19..0; once
+// the digit holding the rem-th key is taken whole, the passes stop there. dh: 256 ints.
+static __device__ void rank_boundary(const uint32_t* a, const uint16_t* ch, int n, uint32_t b1, int rem,
+                              uint32_t* wbits, int* dh, int* wsum, int* sel, const int* cnt = nullptr,
+                              int seg = 0) {
+    // slot i of a segmented list is live if it lies within its segment's count
+    auto live = [&](int i) { return !cnt || (i % seg) < cnt[i / seg]; };
+    const int tid = threadIdx.x;
+    uint32_t P = b1;   // the key bits fixed so far: bits 31..s
+    int s = 20;
+    bool take_all = false;
+    for (int pass = 0; pass < 3 && !take_all; ++pass) {
+        const int sh = pass == 0 ? 12 : (pass == 1 ? 4 : 0);
+        const int nbins = 1 << (s - sh);
+        for (int i = tid; i < 256; i += NT) dh[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += NT) {
+            const uint32_t key = a[i];
+            if (live(i) && (key >> s) == P) atomicAdd(&dh[(key >> sh) & (nbins - 1)], 1);
+        }
+        __syncthreads();
+        if (tid < 32) warp_find_digit(dh, nbins, rem, sel);
+        __syncthreads();
+        rem -= sel[1];
+        P = (P << (s - sh)) | static_cast<uint32_t>(sel[0]);
+        take_all = sel[2] == rem;
+        s = sh;
+    }
+    // winners: above P at bit s; equal to it: all of them, or (ties of whole keys) the first rem
+    if (take_all) {
+        for (int i = tid; i < n; i += NT) {
+            const uint32_t key = a[i];
+            if (live(i) && (key >> 20) == b1 && (key >> s) >= P) {
+                const int c = ch ? ch[i] : i;
+                atomicOr(&wbits[c >> 5], 1u << (c & 31));
+            }
+        }
+        return;
+    }
+    const int R = (n + NT - 1) / NT;
+    const int lo = tid * R < n ? tid * R : n, hi = lo + R < n ? lo + R : n;
+    int eq = 0;
+    for (int i = lo; i < hi; ++i) eq += live(i) && a[i] == P;
+    int eq_all;
+    int r = block_exclusive_scan<NT>(eq, wsum, eq_all);
+    for (int i = lo; i < hi; ++i) {
+        if (!live(i)) continue;
+        const uint32_t key = a[i];
+        bool win = (key >> 20) == b1 && key > P;
+        if (key == P) win = r++ < rem;
+        if (win) {
+            const int c = ch ? ch[i] : i;
+            atomicOr(&wbits[c >> 5], 1u << (c & 31));
+        }
+    }
+}
+
+// Shared memory of the top-k inside the region (bytes from its start).
+constexpr int kTopkDigitsOff = 2048 * 4;   // the 256 digit counts, after the layer histogram
+inline __host__ __device__ size_t topk_region_bytes(int F) {
+    return kTopkKeysOff + static_cast<size_t>(F) * 4 + static_cast<size_t>(kCandCap) * 6 +
+           static_cast<size_t>(F / 32) * 4 + 2 * NW * 4;
+}
+
+// The layer's top-k, taken by every block on its own from the salience and the histogram in
+// global memory (one bulk copy of each). Channels in bins above b1, the bin of the k-th largest
+// key, are taken for sure; the candidates of bin b1 are collected in channel order and ranked
+// among themselves (rank_boundary marks the winners in a channel bitmap). Writes the block's
+// slice [e0, e0 + nloc) of the ascending mask to s_list (and to p.idx if asked). Warp w reads
+// the keys' quads [F/4 w / NW, F/4 (w + 1) / NW), lanes on consecutive quads; the passes over
+// the keys are branch-free (a quad's four channels share one bitmap word).
+static __device__ void layer_topk(const FusedParams& p, unsigned char* region, uint64_t* kbar,
+                                  int* wsum, int* sel, int* s_list, int e0, int nloc) {
+    const int F = p.F, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int* h2 = reinterpret_cast<int*>(region);                                     // [2048]
+    int* dh = reinterpret_cast<int*>(region + kTopkDigitsOff);                    // [256]
+    uint32_t* keys = reinterpret_cast<uint32_t*>(region + kTopkKeysOff);          // [F]
+    uint32_t* ck = keys + F;                                                      // [kCandCap]
+    uint16_t* cch = reinterpret_cast<uint16_t*>(ck + kCandCap);                   // [kCandCap]
+    uint32_t* wbits = reinterpret_cast<uint32_t*>(cch + kCandCap);                // [F / 32]
+    int* wa = reinterpret_cast<int*>(wbits + (F >> 5));                           // [2 NW]
+    if (tid == 0) {
+        mbar_arrive_expect_tx(kbar, static_cast<uint32_t>(F) * 4u + 2048u * 4u);
+        bulk_g2s(keys, p.sigma, static_cast<uint32_t>(F) * 4u, kbar);
+        bulk_g2s(h2, p.ctl->hist, 2048u * 4u, kbar);
+    }
+    for (int i = tid; i < (F >> 5); i += NT) wbits[i] = 0u;
+    mbar_wait(kbar, 0u, p.spin, p.status);
+    block_find_bin<NT>(h2, 2048, p.k, wsum, sel);
+    const uint32_t b1 = static_cast<uint32_t>(sel[0]);
+    const int rem = p.k - sel[1], nb1 = sel[2];
+    const bool whole = nb1 == rem;   // every key of bin b1 is taken
+    const int nq = F >> 2;
+    const int qa = nq * warp / NW, qb = nq * (warp + 1) / NW;
+    const uint4* k4p = reinterpret_cast<const uint4*>(keys);
+    // pass 1: each warp counts its sure keys (bins above b1) and lists its candidates (bin b1)
+    // in channel order in its own segment of the candidate area (ballots give the places)
+    constexpr int seg = kCandCap / NW;
+    const uint32_t lt = (1u << lane) - 1u;
+    int ns = 0, nc = 0;
+    for (int q0 = qa; q0 < qb; q0 += 32) {
+        const int q = q0 + lane;
+        const bool valid = q < qb;
+        const uint4 v = valid ? k4p[q] : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t kk[4] = {v.x, v.y, v.z, v.w};
+        bool f[4];
+        uint32_t m[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ns += valid && (kk[e] >> 20) > b1;
+            f[e] = valid && (kk[e] >> 20) == b1;
+            m[e] = __ballot_sync(0xffffffffu, f[e]);
+        }
+        int pos = nc + __popc(m[0] & lt) + __popc(m[1] & lt) + __popc(m[2] & lt) + __popc(m[3] & lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (f[e] && pos < seg) {
+                ck[warp * seg + pos] = kk[e];
+                cch[warp * seg + pos] = static_cast<uint16_t>(4 * q + e);
+            }
+            pos += f[e];
+        }
+        nc += __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+    }
+    ns = warp_sum(ns);
+    if (lane == 0) {
+        wa[warp] = nc;
+        wa[NW + warp] = ns;
+    }
+    __syncthreads();
+    if (!whole) {
+        bool listed = true;   // every warp's candidates fit its segment
+        for (int w = 0; w < NW; ++w) listed = listed && wa[w] <= seg;
+        if (listed) {
+            rank_boundary(ck, cch, NW * seg, b1, rem, wbits, dh, wsum, sel, wa, seg);
+        } else {
+            rank_boundary(keys, nullptr, F, b1, rem, wbits, dh, wsum, sel);   // many near-equal keys
+        }
+        __syncthreads();
+    }
+    // each warp's taken count: its sure keys plus its winners (or its whole bin-b1 share)
+    int won = wa[warp];
+    if (!whole) {
+        const int c0 = 4 * qa, c1 = 4 * qb;   // the warp's channels [c0, c1)
+        int n = 0;
+        for (int wd = (c0 >> 5) + lane; wd <= ((c1 - 1) >> 5); wd += 32) {
+            uint32_t m = wbits[wd];
+            const int lo = wd * 32;
+            if (lo < c0) m &= ~0u << (c0 - lo);
+            if (lo + 32 > c1) m &= (c1 - lo) >= 32 ? ~0u : ((1u << (c1 - lo)) - 1u);
+            n += __popc(m);
+        }
+        won = warp_sum(n);
+    }
+    __syncthreads();   // every warp has read wa[warp]
+    if (lane == 0) wa[warp] = wa[NW + warp] + won;
+    __syncthreads();
+    int base = 0, total = 0;
+    for (int w = 0; w < NW; ++w) {
+        const int v = wa[w];
+        base += w < warp ? v : 0;
+        total += v;
+    }
+    if (tid == 0 && total != p.k) set_status(p.status, PROX_ERR_BOUNDS);
+    // pass 3: every taken channel's place in the ascending mask (ballots give the places)
+    const uint32_t all_b1 = whole ? 0xFu : 0u;
+    for (int q0 = qa; q0 < qb; q0 += 32) {
+        const int q = q0 + lane;
+        uint32_t tm = 0u;   // bit e: channel 4 q + e is taken
+        if (q < qb) {
+            const uint4 v = k4p[q];
+            const uint32_t wb = ((wbits[q >> 3] >> ((4 * q) & 31)) | all_b1) & 0xFu;
+            const uint32_t b[4] = {v.x >> 20, v.y >> 20, v.z >> 20, v.w >> 20};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                tm |= static_cast<uint32_t>((b[e] > b1) | ((b[e] == b1) & ((wb >> e) & 1u))) << e;
+        }
+        uint32_t m[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m[e] = __ballot_sync(0xffffffffu, (tm >> e) & 1u);
+        int pos = base + __popc(m[0] & lt) + __popc(m[1] & lt) + __popc(m[2] & lt) + __popc(m[3] & lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (((tm >> e) & 1u) && pos >= e0 && pos < e0 + nloc) {
+                s_list[pos - e0] = 4 * q + e;
+                if (p.write_idx) p.idx[pos] = 4 * q + e;
+            }
+            pos += (tm >> e) & 1u;
+        }
+        base += __popc(m[0]) + __popc(m[1]) + __popc(m[2]) + __popc(m[3]);
+    }
+}
+
 // ------------------------------------------------------------------ 5. Stage 2
 
 struct S2Smem {
@@ -684,140 +918,13 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     }
 
     if (select) {
-        // every block takes the whole top-k itself, from the layer's salience and histogram
-        // (one round of loads), and keeps the slice [e0, e1) of the ascending mask that is its
-        // Stage-2 share (writing that slice of the mask out as well)
-        uint32_t* s_skey = reinterpret_cast<uint32_t*>(region + kTopkKeysOff);   // [F]
-        int* h2 = reinterpret_cast<int*>(region);                                  // [2][2048]
+        // every block takes the whole top-k itself and keeps the slice [e0, e1) of the
+        // ascending mask that is its Stage-2 share (writing that slice of the mask out as well)
         grid_wait(&p.ctl->bar, bar1_target, s_flag, p.spin, p.status);   // (1) salience complete
         const int e0 = static_cast<int>(static_cast<long long>(p.k) * blk / P);
         const int e1 = static_cast<int>(static_cast<long long>(p.k) * (blk + 1) / P);
         nloc = min(e1 - e0, kListMax);
-        const int run = select_run(F, NT);
-        auto topk = [&](auto run_c) {
-            constexpr int RUNK = decltype(run_c)::value;
-            constexpr int R4 = RUNK / 4;
-            const int nf4 = F >> 2;
-            // the salience (bulk copy into the candidate area, then into the swizzled runs)
-            // and the histogram (bulk copy), completing on one barrier
-            uint4* stage = reinterpret_cast<uint4*>(region + kTopkKeysOff + 4 * F);
-            if (p.bulk_sigma) {
-                uint64_t* kbar = full + kTopkBar;   // its own barrier, used once per launch
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(kbar, static_cast<uint32_t>(F) * 4u + 2048u * 4u);
-                    bulk_g2s(stage, p.sigma, static_cast<uint32_t>(F) * 4u, kbar);
-                    bulk_g2s(h2, p.ctl->hist, 2048u * 4u, kbar);
-                }
-                mbar_wait(kbar, 0u, p.spin, p.status);
-                for (int u = tid; u < nf4; u += NT)   // thread u / R4's run, swizzled
-                    reinterpret_cast<uint4*>(s_skey)[key_quad<RUNK, true>(u / R4, u % R4)] = stage[u];
-            } else {   // no room for a staging copy: straight from L2 into the runs
-                for (int u = tid; u < nf4; u += NT)
-                    reinterpret_cast<uint4*>(s_skey)[key_quad<RUNK, true>(u / R4, u % R4)] =
-                        __ldcg(reinterpret_cast<const uint4*>(p.sigma) + u);
-                for (int i = tid; i < 2048; i += NT) h2[i] = __ldcg(&p.ctl->hist[i]);
-            }
-            __syncthreads();
-            // the bin b1 of the k-th largest key: keys in higher bins are taken for sure
-            block_find_bin<NT>(h2, 2048, p.k, wsum, sel);
-            const uint32_t b1 = static_cast<uint32_t>(sel[0]);
-            const int above = sel[1], nb1 = sel[2];
-            __syncthreads();
-            const int rem = p.k - above;   // keys to take from bin b1, 1 <= rem <= nb1
-            const int lo = tid * RUNK;
-            const int nv = lo < F ? min(RUNK, F - lo) : 0;
-            uint64_t sure_m = 0ull, cand_m = 0ull;
-#pragma unroll
-            for (int i4 = 0; i4 < R4; ++i4) {
-                if (4 * i4 >= nv) break;   // past the keys (threads beyond F / RUNK own none)
-                const uint4 kk = reinterpret_cast<const uint4*>(s_skey)[key_quad<RUNK, true>(tid, i4)];
-                const uint32_t k4[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int i = 4 * i4 + m;
-                    if (i < nv) {
-                        const uint32_t bin = k4[m] >> 20;
-                        if (bin > b1) sure_m |= 1ull << i;
-                        else if (bin == b1) cand_m |= 1ull << i;
-                    }
-                }
-            }
-            uint64_t take_m = sure_m;
-            if (nb1 == rem) {
-                take_m |= cand_m;   // the whole bin is taken
-            } else {
-                // the candidates (bin b1) in index order, ranked among themselves
-                int n_c;
-                const int c_off = block_exclusive_scan<NT>(__popcll(cand_m), wsum, n_c);
-                if (n_c <= kCandCap) {
-                    uint32_t* ck = reinterpret_cast<uint32_t*>(region + kTopkKeysOff + 4 * F);
-                    unsigned char* tk = region + kTopkKeysOff + 4 * F + kCandCap * 4;
-                    int j = c_off;
-                    for (uint64_t m = cand_m; m; m &= m - 1) {
-                        const int i = __ffsll(static_cast<long long>(m)) - 1;
-                        ck[j++] = s_skey[4 * key_quad<RUNK, true>(tid, i >> 2) + (i & 3)];
-                    }
-                    const int n4 = (n_c + 3) & ~3;
-                    if (tid < n4 - n_c) ck[n_c + tid] = 0u;   // zero keys rank after every real one
-                    __syncthreads();
-                    if (n_c <= kCandDirect) {
-                        // rank of candidate c = candidates ahead of it (larger key, or equal key
-                        // and lower channel: the candidates are in channel order)
-                        for (int c = tid; c < n_c; c += NT) {
-                            const uint32_t kc = ck[c];
-                            int r = 0;
-                            for (int q = 0; q < n_c; ++q) {
-                                const uint32_t kq = ck[q];
-                                r += (kq > kc) || (kq == kc && q < c);
-                            }
-                            tk[c] = r < rem;
-                        }
-                    } else {
-                    auto rank = [&](auto rc_c) {
-                        constexpr int RC = decltype(rc_c)::value;
-                        uint32_t T;
-                        int take_eq, eq_total;
-                        block_select_kth<NT, RC>(ck, n4, rem, h2, wsum, T, take_eq, eq_total);
-                        uint64_t cm;
-                        block_take_topk<NT, RC>(ck, n4, T, take_eq, eq_total, wsum, cm);
-#pragma unroll
-                        for (int i = 0; i < RC; ++i)
-                            if (tid * RC + i < n4) tk[tid * RC + i] = (cm >> i) & 1ull;
-                    };
-                    const int rc = select_run(n4, NT);
-                    if (rc <= 4) rank(std::integral_constant<int, 4>());
-                    else rank(std::integral_constant<int, 8>());
-                    }
-                    __syncthreads();
-                    j = c_off;
-                    for (uint64_t m = cand_m; m; m &= m - 1) {
-                        const int i = __ffsll(static_cast<long long>(m)) - 1;
-                        if (tk[j++]) take_m |= 1ull << i;
-                    }
-                } else {
-                    // many equal or near-equal saliences: rank over every key instead
-                    uint32_t T;
-                    int take_eq, eq_total;
-                    block_select_kth<NT, RUNK, true>(s_skey, F, p.k, h2, wsum, T, take_eq, eq_total,
-                                                     nullptr, true);
-                    block_take_topk<NT, RUNK, true>(s_skey, F, T, take_eq, eq_total, wsum, take_m);
-                }
-            }
-            int total;
-            int pos = block_exclusive_scan<NT>(__popcll(take_m), wsum, total);
-            if (tid == 0 && total != p.k) set_status(p.status, PROX_ERR_BOUNDS);
-            for (uint64_t m = take_m; m && pos < e0 + nloc; m &= m - 1, ++pos) {
-                const int i = __ffsll(static_cast<long long>(m)) - 1;
-                if (pos >= e0) {
-                    s_list[pos - e0] = lo + i;
-                    if (p.write_idx) p.idx[pos] = lo + i;
-                }
-            }
-        };
-        if (run <= 8) topk(std::integral_constant<int, 8>());
-        else if (run <= 16) topk(std::integral_constant<int, 16>());
-        else if (run <= 32) topk(std::integral_constant<int, 32>());
-        else topk(std::integral_constant<int, 64>());
+        layer_topk(p, region, full + kTopkBar, wsum, sel, s_list, e0, nloc);
         __syncthreads();
         if (!(p.mode & kFusedStage2) && tid == 0) {
             // no later barrier: the last block to have read the histogram clears it
@@ -892,7 +999,6 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
 
 struct FusedShape {
     int RUN, CW, CPTMAX, NG, WPG, CPT, nstage_log2;
-    bool bulk_sigma;
     size_t region, smem;
 };
 
@@ -921,7 +1027,6 @@ inline bool fused_shape(int d, int F, int sms, FusedShape& s, size_t row_bytes) 
     if ((F + sms - 1) / sms > kListMax) return false;
     s.RUN = select_run(d, NT);
     if (s.RUN > 16) return false;
-    if (select_run(F, NT) > 64) return false;   // the per-block top-k holds 64 keys a thread
     s.CW = nch_max <= 4 ? 4 : (nch_max <= 8 ? 8 : 16);
     s.nstage_log2 = fused_nstage_log2(row_bytes);
     const int nstage = 1 << s.nstage_log2;
@@ -951,12 +1056,8 @@ inline bool fused_shape(int d, int F, int sms, FusedShape& s, size_t row_bytes) 
     const size_t p3 = static_cast<size_t>(NT) * 16 + 2048 * 4;  // parts + histogram
     if (p3 > p1) p1 = p3;
     size_t region = offP1 + p1;
-    const size_t p4 = kTopkKeysOff + static_cast<size_t>(F) * 4 + kCandCap * 5;
+    const size_t p4 = topk_region_bytes(F);
     if (p4 > region) region = p4;
-    // with room for a staging copy of the salience next to the keys, it comes in one bulk copy
-    const size_t p4b = kTopkKeysOff + static_cast<size_t>(F) * 8;
-    s.bulk_sigma = align_up(p4b > region ? p4b : region, 128) + kFixedSmem <= kMaxSmem;
-    if (s.bulk_sigma && p4b > region) region = p4b;
     const size_t ring = static_cast<size_t>(nstage) * row_bytes;
     if (ring > region) region = ring;
     const size_t scratch = static_cast<size_t>(s.NG) * d * 4 > 32 * 16 * 16
