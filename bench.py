@@ -67,6 +67,9 @@ def parse(argv=None):
                     help="Stage-2 rows as FP8 E4M3 with row scales (single token only)")
     ap.add_argument("--spread-ms", type=float, default=300.0,
                     help="wall time of the extra chunked run that gives the p10/p50/p90 spread")
+    ap.add_argument("--window", type=int, default=None,
+                    help="32-layer stack only: keep the Stage-1 proxies in pinned host memory "
+                         "and page them through this many device slots (prox_window_*)")
     return ap.parse_args(argv)
 
 
@@ -717,12 +720,109 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_window(args):
+    """The 32-layer stack with the proxy memory reduced to a sliding window of `args.window`
+    device slots (split layers, proxies paged in from pinned host memory on the window's
+    copy stream), against the same stack with resident layers. Steps are launched from the host
+    (the window's slot state lives on the host), K steps timed with CUDA events on the compute
+    stream. Rank 0 prints one JSON line."""
+    import torch
+
+    import free_sparse_swiglu_stage1_b300 as P
+    import workloads as WL
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    cfg = resolve(args)
+    if not cfg["chain"]:
+        raise SystemExit("--window needs the 32-layer stack (--workload 4)")
+    B, sp, s_in = cfg["batch"], cfg["sparsity"], cfg["input_sparsity"]
+    d, F, depth = cfg["d"], cfg["F"], cfg["depth"]
+    S = args.window
+    full, split = [], []
+    for li in range(depth):
+        mats = WL.make_layer(cfg["key"], li)
+        dev = {n: v.cuda() for n, v in mats.items() if n.startswith("w_")}
+        lay = P.prox_pack_weights(dev["w_gate"], dev["w_up"], dev["w_down"])
+        full.append(lay)
+        split.append(P.prox_split_packed(lay, proxy_on_host=True))
+        del dev
+    win = P.ProxyWindow(split, S)
+    T = max(B, args.tokens // B * B)
+    X = torch.from_numpy(WL.make_tokens(cfg["key"], range(rank * T, (rank + 1) * T))).cuda()
+    Xa = torch.empty((2, B, d), dtype=torch.float32, device="cuda")
+    Ya = torch.empty((B, d), dtype=torch.float32, device="cuda")
+    ws = P.prox_workspace(d, F, B)
+    stream = torch.cuda.Stream()
+    nb = T // B
+
+    def step(i, windowed):
+        t = i % nb
+        xin = X[t * B:(t + 1) * B]
+        for li in range(depth):
+            desc = win.acquire(li, stream=stream) if windowed else full[li]
+            P.prox_ffn_forward(desc, xin, sp, s_in, ws, y=Ya, stream=stream)
+            if windowed:
+                win.release(li, stream=stream)
+            P.prox_rmsnorm(Ya, 1e-6, out=Xa[li % 2], stream=stream)
+            xin = Xa[li % 2]
+
+    def timed(windowed, K):
+        for i in range(max(3, args.warmup)):
+            step(i, windowed)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0 = win.stats()
+        n0 = P.prox_launch_count()
+        e0.record(stream)
+        for i in range(K):
+            step(i, windowed)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        c1 = win.stats()
+        return (e0.elapsed_time(e1) / 1000.0, c1[0] - c0[0], c1[1] - c0[1],
+                P.prox_launch_count() - n0)
+
+    K = args.steps
+    t_res, _, _, _ = timed(False, K)
+    sampler = ClockSampler(None)
+    sampler.start()
+    time.sleep(0.3)
+    t_win, copies, h2d, launches = timed(True, K)
+    clocks = sampler.stop()
+    st = P.prox_get_status(ws, stream=stream)
+    if st != 0:
+        raise RuntimeError(f"device status: {P.prox_error_string(st)}")
+    pb = P.prox_proxy_bytes(d, F)
+    units = K * B * depth
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": units / t_win, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": 1000.0 * t_win / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(workload_config(cfg, world, T, P.prox_k_for(sp, F), P.prox_k_for(s_in, d)),
+                           proxy_window=S, launch="host-driven (no CUDA graph)"),
+            "us_per_layer": 1e6 * t_win / (K * depth),
+            "resident_us_per_layer": 1e6 * t_res / (K * depth),
+            "window": {"slots": S, "proxy_bytes_per_layer": pb,
+                       "proxy_device_bytes": S * pb, "proxy_device_bytes_resident": depth * pb,
+                       "copies_per_step": copies / K, "h2d_bytes_per_step": h2d / K,
+                       "h2d_gbs": h2d / t_win / 1e9},
+            "gpu_launches": launches, "clocks": clocks, "e2e": None,
+            "e2e_note": "the window's proxies come from host memory on every visit; the device "
+                        "input and output stay resident"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.steps is None:
         args.steps = 400 if args.workload == CHAIN_WORKLOAD else 20000
     if args.impl == "reference":
         run_reference(args)
+    elif args.window is not None:
+        run_window(args)
     else:
         run_ours(args)
 
