@@ -121,8 +121,8 @@ int launch_fused(const uint8_t* packed, const PackedLayout& L, int d, int F, con
     p.WPG = sh.WPG;
     p.CPT = sh.CPT;
     p.write_idx = c.write_idx ? 1 : 0;
-    // the code array must fit L2 several times over (126 MB on B300) to stay there
-    p.prefetch_codes = 0;   // measured slower on the 4096 x 14336 layer: it delays the x loads
+    // the early hint pays while the likely-kept proxy rows fit L2 (126 MB) with room to spare
+    p.prefetch_codes = static_cast<size_t>(c.k_in) * F <= (static_cast<size_t>(48) << 20) ? 1 : 0;
     p.dbg_qx = c.dbg_qx;
     p.dbg_sx = c.dbg_sx;
     p.dbg_gate = c.dbg_gate;

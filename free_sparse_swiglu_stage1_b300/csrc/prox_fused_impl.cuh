@@ -37,7 +37,7 @@ struct FusedParams {
     long long spin;
     int region_bytes, nstage_log2, NG, WPG, CPT;
     int write_idx;   // also store the mask into idx (the caller asked for it)
-    int prefetch_codes;   // bring the whole proxy code array into L2 at the start
+    int prefetch_codes;   // ask L2 for the likely-kept proxy rows during the input selection
     int8_t* dbg_qx;
     float* dbg_sx;
     int32_t* dbg_gate;
@@ -183,10 +183,27 @@ __device__ void select_inputs(const FusedParams& p, uint32_t* keys, int* hist, i
                 make_uint4(__float_as_uint(v.x) & 0x7fffffffu, __float_as_uint(v.y) & 0x7fffffffu,
                            __float_as_uint(v.z) & 0x7fffffffu, __float_as_uint(v.w) & 0x7fffffffu);
     }
+    // first radix pass here (counts of the keys' bits 30..20): inputs in bins at or above the
+    // bin of the k_in-th largest are a superset of the kept ones, so each block can already ask
+    // L2 for its share of those proxy rows (rows blk, blk + P, ...) while the selection finishes
+    // and HBM would otherwise idle; a hint only
+    for (int i = tid; i < 2048; i += NT) hist[i] = 0;
     __syncthreads();
+    if (active)
+#pragma unroll
+        for (int e = 0; e < RUN; ++e) atomicAdd(&hist[(__float_as_uint(xv[e]) & 0x7fffffffu) >> 20], 1);
+    __syncthreads();
+    if (p.prefetch_codes) {
+        int* sel = wsum + NW;
+        block_find_bin<NT>(hist, 2048, p.k_in, wsum, sel);
+        const uint32_t b1 = static_cast<uint32_t>(sel[0]);
+        const int r = blockIdx.x + tid * gridDim.x;
+        if (r < d && ((__float_as_uint(__ldg(p.x + r)) & 0x7fffffffu) >> 20) >= b1)
+            prefetch_l2(p.codes + static_cast<size_t>(r) * p.F, static_cast<uint32_t>(p.F));
+    }
     uint32_t T;
     int take, eq_total;
-    block_select_kth<NT, RUN, true>(keys, d, p.k_in, hist, wsum, T, take, eq_total);
+    block_select_kth<NT, RUN, true>(keys, d, p.k_in, hist, wsum, T, take, eq_total, nullptr, true);
     uint64_t mine;
     block_take_topk<NT, RUN, true>(keys, d, T, take, eq_total, wsum, mine);
     // the group's scale: its largest kept magnitude / 127
@@ -875,13 +892,6 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     const bool select = (p.mode & kFusedSelect) != 0;
     if (stage1 && tid < G && nch > 0)   // the tile's scales, needed after the GEMV
         prefetch_l2(p.scales + static_cast<size_t>(tid) * F + c0, static_cast<uint32_t>(nch) * 64u);
-    if (stage1 && p.prefetch_codes && tid == NT - 1) {
-        // while every block selects the inputs, HBM would idle: bring the whole code array
-        // into L2 (block blk takes the contiguous rows [d blk / P, d (blk + 1) / P)), so the
-        // GEMV's scattered kept-row reads hit L2; rejected rows cost DRAM bytes, not time
-        const size_t r0 = static_cast<size_t>(d) * blk / P, r1 = static_cast<size_t>(d) * (blk + 1) / P;
-        if (r1 > r0) prefetch_l2(p.codes + r0 * F, static_cast<uint32_t>((r1 - r0) * F));
-    }
     __syncthreads();
 
     int nloc = 0;
@@ -903,14 +913,18 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
             bar1_target = grid_arrive(&p.ctl->bar, s_target);   // (1) arrive; wait below
         }
         if (select && (p.mode & kFusedStage2) && nchan > 0) {
-            // while the mask is being agreed on, bring the rows of the tile's most salient
-            // channels (those above the bin of its M-th largest, M = 60% of the tile's
-            // expected share of the mask) into L2, so HBM keeps streaming; a hint only
+            // while the mask is being agreed on, bring the rows of the tile's M most salient
+            // channels (M = 60% of the tile's expected share of the mask) into L2, so HBM keeps
+            // streaming; a hint only. A channel's rank in its tile is counted directly.
             const int M = static_cast<int>(0.6 * static_cast<double>(p.k) * nchan / F);
-            if (M >= 1) {
-                block_find_bin<NT>(s_hist, 2048, M, wsum, sel);
-                const uint32_t bt = static_cast<uint32_t>(sel[0]);
-                if (tid < nchan && (s_key[tid] >> 20) > bt)
+            if (tid < nchan && M >= 1) {
+                const uint32_t key = s_key[tid];
+                int above = 0;
+                for (int j = 0; j < nchan; ++j) {
+                    const uint32_t kj = s_key[j];
+                    above += kj > key || (kj == key && j < tid);
+                }
+                if (above < M)
                     prefetch_l2(reinterpret_cast<const unsigned char*>(p.rows) + static_cast<size_t>(c0 + tid) * p.row_bytes,
                                 static_cast<uint32_t>(p.row_bytes));
             }
