@@ -67,6 +67,9 @@ def parse(argv=None):
                     help="Stage-2 rows as FP8 E4M3 with row scales (single token only)")
     ap.add_argument("--spread-ms", type=float, default=300.0,
                     help="wall time of the extra chunked run that gives the p10/p50/p90 spread")
+    ap.add_argument("--allocate", type=float, nargs="*", default=None,
+                    help="fit the path's cost model to measured times, then time the sparsity "
+                         "allocation prox_choose_sparsity picks for these target effective sparsities")
     ap.add_argument("--window", type=int, default=None,
                     help="32-layer stack only: keep the Stage-1 proxies in pinned host memory "
                          "and page them through this many device slots (prox_window_*)")
@@ -720,6 +723,82 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_allocate(args):
+    """Sparsity allocation with a measured cost model: the single-token path is timed at a few
+    (k_in, k) points and the dense FFN once; prox_cost_model_fit turns those times into the
+    cost model (microseconds), prox_choose_sparsity picks (input sparsity, sparsity) for each
+    target effective sparsity, and the path is timed at that choice, so the achieved effective
+    sparsity 1 - t / t_dense stands beside the predicted one. The byte cost model's choice is
+    timed the same way. Rank 0 prints one JSON line."""
+    import torch
+
+    import free_sparse_swiglu_stage1_b300 as P
+    import workloads as WL
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    cfg = resolve(args)
+    if cfg["chain"] or cfg["batch"] != 1:
+        raise SystemExit("--allocate times one layer at batch 1")
+    d, F, L = cfg["d"], cfg["F"], cfg["layers"]
+    layers = []
+    for li in range(L):
+        mats = WL.make_layer(cfg["key"], li)
+        dev = {n: v.cuda() for n, v in mats.items() if n.startswith("w_")}
+        layers.append(P.prox_pack_weights(dev["w_gate"], dev["w_up"], dev["w_down"]))
+        del dev
+    T = args.tokens
+    X = torch.from_numpy(WL.make_tokens(cfg["key"], range(T))).cuda()
+    Y = torch.empty((1, d), dtype=torch.float32, device="cuda")
+    ws = P.prox_workspace(d, F, 1)
+    stream = torch.cuda.Stream()
+    K = args.steps
+
+    def time_steps(fn):
+        with torch.cuda.stream(stream):
+            for i in range(max(3, args.warmup)):
+                fn(i)
+        torch.cuda.synchronize()
+        g = capture(torch, stream, fn, K)
+        with torch.cuda.stream(stream):
+            g.replay()
+        return timed_graph_replays(torch, stream, [g], lambda: None, "allocate") / K * 1e6
+
+    def path_us(s_in, s):
+        return time_steps(lambda i: P.prox_ffn_forward(layers[i % L], X[(i // L) % T][None], s, s_in,
+                                                       ws, y=Y, stream=stream))
+
+    dense = time_steps(lambda i: P.prox_dense_ffn(layers[i % L], X[(i // L) % T][None], ws, y=Y,
+                                                  stream=stream))
+    pts = [(0.5, 0.7), (0.0, 0.7), (0.5, 0.4), (0.7, 0.9), (0.3, 0.55)]
+    meas = []
+    for s_in, s in pts:
+        meas.append({"input_sparsity": s_in, "sparsity": s, "k_in": P.prox_k_for(s_in, d),
+                     "k": P.prox_k_for(s, F), "us": path_us(s_in, s)})
+    model = P.prox_cost_model_fit([m["k_in"] for m in meas], [m["k"] for m in meas],
+                                  [m["us"] for m in meas], dense, 1e-6)
+    byte_model = P.prox_cost_model_bytes(d, F)
+    out = []
+    for tgt in args.allocate:
+        for name, cm in (("measured", model), ("bytes", byte_model)):
+            try:
+                s1, s2, pred = P.prox_choose_sparsity(cm, d, F, tgt)
+            except P.ProxError as e:
+                out.append({"target": tgt, "model": name, "error": str(e)})
+                continue
+            t = path_us(s1, s2)
+            out.append({"target": tgt, "model": name, "input_sparsity": s1, "sparsity": s2,
+                        "k_in": P.prox_k_for(s1, d), "k": P.prox_k_for(s2, F),
+                        "predicted_effective": pred, "us": t, "achieved_effective": 1.0 - t / dense})
+    if rank != 0:
+        return
+    print(json.dumps({"workload": cfg["name"], "d_model": d, "d_ff": F, "steps_per_point": K,
+                      "dense_us": dense, "measurements": meas,
+                      "fitted_model_us": {"in_cost": model.in_cost, "fixed_cost": model.fixed_cost,
+                                          "ch_cost": model.ch_cost, "dense_cost": model.dense_cost},
+                      "allocations": out}), flush=True)
+
+
 def run_window(args):
     """The 32-layer stack with the proxy memory reduced to a sliding window of `args.window`
     device slots (split layers, proxies paged in from pinned host memory on the window's
@@ -823,6 +902,8 @@ def main():
         run_reference(args)
     elif args.window is not None:
         run_window(args)
+    elif args.allocate is not None:
+        run_allocate(args)
     else:
         run_ours(args)
 

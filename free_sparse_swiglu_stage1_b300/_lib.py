@@ -68,6 +68,7 @@ SIGNATURES = {
     "prox_debug_fused_forward": (_i, [_P, _vp, _d, _d, _vp, _vp, _vp, _sz, _vp]),
     "prox_debug_wait_timeout": (_i, [_vp, _sz, ctypes.c_longlong, _vp]),
     "prox_proxy_bytes": (_sz, [_i, _i, _i]),
+    "prox_cost_model_fit": (_i, [_vp, _vp, _vp, _i, _d, _d, ctypes.POINTER(prox_cost_model)]),
     "prox_rows_bytes": (_sz, [_i, _i, _i, _i]),
     "prox_split_packed": (_i, [_P, _vp, _sz, _vp, _sz, _vp, _P]),
     "prox_window_create": (_i, [_i, _i, _i, _i, ctypes.POINTER(_vp), _vp, _sz,

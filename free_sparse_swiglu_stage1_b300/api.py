@@ -65,6 +65,19 @@ def prox_cost_model_bytes(d_model: int, d_ff: int) -> prox_cost_model:
     return out
 
 
+def prox_cost_model_fit(k_in, k, t, dense_t: float, min_cost: float = 1e-9) -> prox_cost_model:
+    """The cost model t = in_cost k_in + fixed_cost + ch_cost k fitted to measured times."""
+    n = len(t)
+    if len(k_in) != n or len(k) != n:
+        raise ValueError("k_in, k and t must have the same length")
+    arr = lambda v: (ctypes.c_double * max(n, 1))(*[float(x) for x in v])
+    out = prox_cost_model()
+    _lib.check(_lib.lib().prox_cost_model_fit(arr(k_in), arr(k), arr(t), n, float(dense_t),
+                                              float(min_cost), ctypes.byref(out)),
+               "prox_cost_model_fit")
+    return out
+
+
 def prox_choose_sparsity(cost: prox_cost_model, d_model: int, d_ff: int, target: float,
                          anchor: float = 0.7, min_input_kept: float = 0.3):
     """(input_sparsity, sparsity, effective_sparsity) for a target effective sparsity."""
@@ -445,7 +458,7 @@ def prox_debug_wait_timeout(ws: Workspace, spin_cycles: int, stream=None) -> Non
 
 __all__ = [
     "GROUP", "MAX_BATCH", "MAX_TOKENS", "ProxyWindow", "SplitLayer", "prox_proxy_bytes",
-    "prox_rows_bytes", "prox_split_packed", "prox_debug_window_plan", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
+    "prox_rows_bytes", "prox_split_packed", "prox_debug_window_plan", "prox_cost_model_fit", "PackedLayer", "ProxError", "Workspace", "prox_build_mask",
     "prox_choose_sparsity", "prox_cost_model", "prox_cost_model_bytes",
     "prox_debug_fused_forward", "prox_debug_stage1", "prox_debug_union", "prox_debug_wait_timeout", "prox_dense_ffn",
     "prox_error_string", "prox_ffn_forward", "prox_ffn_forward_host", "prox_get_status",

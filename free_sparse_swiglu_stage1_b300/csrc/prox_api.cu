@@ -1,6 +1,7 @@
 // The C ABI declared in include/prox.h: argument validation, buffer carving and the order
 // of launches. Every step of the computation runs in the kernels; this file only decides
 // what to launch, on which stream, with which pointers.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -270,6 +271,54 @@ int prox_cost_model_bytes(int d_model, int d_ff, prox_cost_model* out) {
     out->fixed_cost = 4.0 * G * F;
     out->ch_cost = 6.0 * d;
     out->dense_cost = 6.0 * d * F;
+    return PROX_OK;
+}
+
+int prox_cost_model_fit(const double* k_in, const double* k, const double* t, int n, double dense_t,
+                        double min_cost, prox_cost_model* out) {
+    if (!k_in || !k || !t || !out || n < 3 || !(dense_t > 0.0) || !(min_cost >= 0.0) ||
+        !std::isfinite(dense_t))
+        return PROX_ERR_INVALID_ARG;
+    // normal equations of the fit t ~ a k_in + b + c k, unknowns (a, b, c)
+    double M[3][3] = {{0, 0, 0}, {0, 0, 0}, {0, 0, 0}}, r[3] = {0, 0, 0};
+    for (int i = 0; i < n; ++i) {
+        if (!std::isfinite(k_in[i]) || !std::isfinite(k[i]) || !std::isfinite(t[i]) ||
+            k_in[i] < 0.0 || k[i] < 0.0 || t[i] < 0.0)
+            return PROX_ERR_INVALID_ARG;
+        const double v[3] = {k_in[i], 1.0, k[i]};
+        for (int a = 0; a < 3; ++a) {
+            r[a] += v[a] * t[i];
+            for (int b = 0; b < 3; ++b) M[a][b] += v[a] * v[b];
+        }
+    }
+    // Gaussian elimination with partial pivoting
+    double A[3][4];
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 3; ++b) A[a][b] = M[a][b];
+        A[a][3] = r[a];
+    }
+    double scale = 0.0;
+    for (int a = 0; a < 3; ++a)
+        for (int b = 0; b < 3; ++b) scale = std::max(scale, std::fabs(A[a][b]));
+    for (int col = 0; col < 3; ++col) {
+        int best = col;
+        for (int row = col + 1; row < 3; ++row)
+            if (std::fabs(A[row][col]) > std::fabs(A[best][col])) best = row;
+        if (!(std::fabs(A[best][col]) > 1e-12 * scale)) return PROX_ERR_INVALID_ARG;
+        if (best != col) {
+            for (int b = 0; b < 4; ++b) std::swap(A[col][b], A[best][b]);
+        }
+        for (int row = 0; row < 3; ++row) {
+            if (row == col) continue;
+            const double f = A[row][col] / A[col][col];
+            for (int b = col; b < 4; ++b) A[row][b] -= f * A[col][b];
+        }
+    }
+    const double a = A[0][3] / A[0][0], b = A[1][3] / A[1][1], c = A[2][3] / A[2][2];
+    out->in_cost = std::max(a, min_cost);
+    out->fixed_cost = std::max(b, 0.0);
+    out->ch_cost = std::max(c, min_cost);
+    out->dense_cost = dense_t;
     return PROX_OK;
 }
 

@@ -49,7 +49,7 @@ input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, i
                    int* __restrict__ grows, int* __restrict__ gcnt, int* __restrict__ gq,
                    int8_t* __restrict__ gqx, float* __restrict__ sx_ws, int* __restrict__ ghist,
                    uint32_t* __restrict__ zbits, int F, uint16_t* __restrict__ qxh,
-                   int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx) {
+                   int8_t* __restrict__ dbg_qx, float* __restrict__ dbg_sx, int lists) {
     extern __shared__ __align__(16) unsigned char smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);                 // [d]
     int8_t* qx8 = reinterpret_cast<int8_t*>(keys + d);                   // [TB][d]
@@ -147,6 +147,7 @@ input_quant_kernel(const float* __restrict__ x, int d, int B, int TB, int TBs, i
         __syncthreads();   // keys are rewritten for the next token
     }
     for (int i = tid; i < (TB - nb) * G; i += NT) sx_ws[nb * G + i] = 0.f;
+    if (!lists) return;   // the tensor-core Stage 1 reads the dense codes only
 
     // per group: the inputs any token kept, ascending, then padding to a multiple of 4
     const int cnt = __popcll(any);
@@ -490,19 +491,23 @@ int launch_input_quant(const float* x, int d, int F, int B, int k_in, uint8_t* w
                        const WsLayout& W, uint32_t* zbits, bool dense_codes, int8_t* dbg_qx,
                        float* dbg_sx, cudaStream_t s) {
     if (dense_codes && (W.BPtc == 0 || B > kTcMaxTokens)) return PROX_ERR_UNSUPPORTED;
-    const size_t smem = static_cast<size_t>(d) * 4 + static_cast<size_t>(W.TB) * d;
+    // with dense codes (the tensor-core Stage 1) every token is a block of its own and no
+    // per-tile kept-row lists are built; the per-token outputs (sx [B][G], ghist [B][2048]) keep
+    // their places, the tiles being consecutive tokens
+    const int TB = dense_codes ? 1 : W.TB;
+    const size_t smem = static_cast<size_t>(d) * 4 + static_cast<size_t>(TB) * d;
     const int run = select_run(d, kSelThreads);   // d <= 16384: at most 16
     if (run > 16) return PROX_ERR_UNSUPPORTED;
     auto fn = run <= 4 ? input_quant_kernel<4> : (run <= 8 ? input_quant_kernel<8> : input_quant_kernel<16>);
     if (ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem) != PROX_OK) return PROX_ERR_CUDA;
-    const int ntiles = (B + W.TB - 1) / W.TB;
-    return launch_pdl(fn, dim3(ntiles), dim3(kSelThreads), smem, s, x, d, B, W.TB,
-                      stage1_width(B, W.TB), k_in, reinterpret_cast<int*>(ws + W.grows),
+    const int ntiles = (B + TB - 1) / TB;
+    return launch_pdl(fn, dim3(ntiles), dim3(kSelThreads), smem, s, x, d, B, TB,
+                      stage1_width(B, TB), k_in, reinterpret_cast<int*>(ws + W.grows),
                       reinterpret_cast<int*>(ws + W.gcnt), reinterpret_cast<int*>(ws + W.gq),
                       reinterpret_cast<int8_t*>(ws + W.gqx), reinterpret_cast<float*>(ws + W.sx),
                       reinterpret_cast<int*>(ws + W.ghist), zbits, F,
                       dense_codes ? reinterpret_cast<uint16_t*>(ws + W.qxh) : nullptr, dbg_qx,
-                      dbg_sx);
+                      dbg_sx, dense_codes ? 0 : 1);
 }
 
 template <int TB, int CPL>

@@ -110,6 +110,17 @@ typedef struct prox_cost_model {
  * shape or a NULL out. */
 int prox_cost_model_bytes(int d_model, int d_ff, prox_cost_model* out);
 
+/* A cost model fitted to measured times: the least-squares fit of
+ *   t = in_cost * k_in + fixed_cost + ch_cost * k
+ * over n >= 3 measurements (k_in[i], k[i], t[i]) of the sparse path on one layer shape, with
+ * dense_cost = dense_t (the dense FFN's measured time, same unit). Host-only. Coefficients
+ * that come out below min_cost (noise on a term the path barely depends on) are raised to it,
+ * so the model stays valid for prox_choose_sparsity. PROX_ERR_INVALID_ARG for NULL
+ * pointers, n < 3, non-finite or negative inputs, dense_t <= 0, or measurements whose
+ * (k_in, k) points do not determine the three coefficients. */
+int prox_cost_model_fit(const double* k_in, const double* k, const double* t, int n, double dense_t,
+                        double min_cost, prox_cost_model* out);
+
 /* Sparsity allocation (technical summary, "Sparsity Allocation": the Stage 2 sparsity is
  * anchored around 70%, Stage 1 keeps at least 30% of the inputs, and a cost model chooses the
  * two sparsities for a target effective sparsity, counting the proxy's overhead). The pages

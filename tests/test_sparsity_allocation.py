@@ -142,3 +142,33 @@ def test_library_rejects_bad_arguments():
     assert L.prox_choose_sparsity(ctypes.byref(bad), 256, 64, 0.5, 0.7, 0.3, ctypes.byref(out),
                                   None, None) == -1
     assert L.prox_cost_model_bytes(100, 64, ctypes.byref(cm)) == -1
+
+
+def test_cost_model_fit_recovers_a_linear_model():
+    """The fit against numpy's least squares, on exact and on noisy synthetic measurements."""
+    from free_sparse_swiglu_stage1_b300 import prox_cost_model_fit
+    rng = np.random.default_rng(7)
+    k_in = np.array([2048, 4096, 2048, 1229, 3000, 1500], float)
+    k = np.array([4301, 4301, 8602, 1434, 6000, 3000], float)
+    a, b, c = 2.5e-3, 9.0, 3.1e-3
+    t = a * k_in + b + c * k
+    m = prox_cost_model_fit(k_in, k, t, 60.0)
+    assert math.isclose(m.in_cost, a, rel_tol=1e-9) and math.isclose(m.fixed_cost, b, rel_tol=1e-9)
+    assert math.isclose(m.ch_cost, c, rel_tol=1e-9) and m.dense_cost == 60.0
+    tn = t + rng.normal(0, 0.3, len(t))
+    m = prox_cost_model_fit(k_in, k, tn, 60.0)
+    want = np.linalg.lstsq(np.stack([k_in, np.ones_like(k_in), k], 1), tn, rcond=None)[0]
+    np.testing.assert_allclose([m.in_cost, m.fixed_cost, m.ch_cost], want, rtol=1e-9, atol=1e-12)
+
+
+def test_cost_model_fit_guards():
+    from free_sparse_swiglu_stage1_b300 import ProxError, prox_cost_model_fit
+    # a term the times do not depend on is raised to min_cost, so allocation still accepts it
+    m = prox_cost_model_fit([1, 2, 3, 4], [10, 10, 20, 20], [5, 5, 5, 5], 10.0, min_cost=1e-6)
+    assert m.in_cost == 1e-6 and m.ch_cost == 1e-6 and math.isclose(m.fixed_cost, 5.0)
+    with pytest.raises(ProxError):   # all points on one line: the coefficients are not determined
+        prox_cost_model_fit([1, 2, 3], [1, 2, 3], [1, 2, 3], 10.0)
+    with pytest.raises(ProxError):
+        prox_cost_model_fit([1, 2], [1, 2], [1, 2], 10.0)
+    with pytest.raises(ProxError):
+        prox_cost_model_fit([1, 2, 3], [3, 1, 2], [1, 2, 3], 0.0)
