@@ -184,8 +184,8 @@ int prox_pack_weights(const uint16_t* w_gate, const uint16_t* w_up, const uint16
  * at 448 (both divisions in IEEE binary32), code = 0 if s == 0. Arguments as for
  * prox_pack_weights (packed_bytes >= prox_packed_bytes_fp8); out->format = PROX_FORMAT_FP8.
  * Calls that run Stage 2 on such a layer (prox_sparse_ffn, prox_ffn_forward,
- * prox_ffn_forward_host, prox_dense_ffn) accept one token per call and return
- * PROX_ERR_UNSUPPORTED for a batch; prox_build_mask and prox_debug_stage1 accept any batch. */
+ * prox_ffn_forward_host, prox_dense_ffn) run a batch token by token through the single-token
+ * kernel; prox_build_mask and prox_debug_stage1 are unchanged (Stage 1 reads the proxies). */
 int prox_pack_weights_fp8(const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                           int d_model, int d_ff, int group,
                           void* packed_dev, size_t packed_bytes, void* stream, prox_packed* out);
@@ -217,7 +217,9 @@ int prox_sparse_ffn(const prox_packed* w, const float* x, int batch, const int32
  * Prox Framework": Stage 1 "Lightweight Proxy Construction" builds the shared mask m_s, Stage
  * 2 "Exact Sparse Computation" computes the masked channels exactly; the authors' abstract:
  * all three projections run sparse under the one mask). At sparsity 0 every channel is kept
- * and Stage 1 is skipped (the result is the dense FFN).
+ * and Stage 1 is skipped (the result is the dense FFN). One token runs the whole path in one
+ * launch; two tokens run as two such launches; 3 to 16 tokens run the batch kernels (Stage 2
+ * on the tensor cores over the union of the masks), larger batches 16-token tiles of those.
  *   y       [batch][d_model] fp32 device (written).
  *   idx_out [batch][k] int32 device, or NULL when the mask is not wanted. */
 int prox_ffn_forward(const prox_packed* w, const float* x, int batch,

@@ -4,8 +4,8 @@ Compatibility: Prox is orthogonal to weight quantization such as FP8), through t
 The packed FP8 codes and row scales must equal the oracle's bit for bit; the proxies, hence the
 masks, must be those of the bf16 packing; y must match the oracle's exact Stage 2 over the
 dequantized FP8 weights within the Stage-2 tolerance (the same arithmetic as the bf16 path:
-exact products, fp32 accumulation). Stage 2 over FP8 rows is single-token; a batch is
-refused.
+exact products, fp32 accumulation). Stage 2 over FP8 rows runs in the single-token kernel; a
+batch runs token by token and gives each token's single-token result bit for bit.
 """
 import numpy as np
 import pytest
@@ -84,15 +84,29 @@ def test_fp8_given_mask_and_forward(layer):
     assert P.prox_get_status(ws) == 0
 
 
-def test_fp8_dense_and_refusals(layer):
-    ws = ws_for(layer, 2)
-    x = WL.make_random_tokens(2, layer.d, seed=80)
+def test_fp8_dense_and_batches(layer):
+    B = 5
+    ws = ws_for(layer, B)
+    x = WL.make_random_tokens(B, layer.d, seed=80)
     yd = P.prox_dense_ffn(layer.packed, cuda(x[:1]), ws).cpu().numpy()[0]
     check_y(yd, O.dense_ffn(x[0], layer.f8["w_gate"], layer.f8["w_up"], layer.f8["w_down"]))
-    with pytest.raises(P.ProxError) as e:
-        P.prox_ffn_forward(layer.packed, cuda(x), 0.7, 0.5, ws)
-    assert e.value.code == -6
-    # masks of a batch need no Stage 2: fine on an FP8 layer
+    # a batch goes token by token: each row equals the single-token call bit for bit
+    k = O.k_for(0.7, layer.F)
+    idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+    y = P.prox_ffn_forward(layer.packed, cuda(x), 0.7, 0.5, ws, idx_out=idx)
+    ydb = P.prox_dense_ffn(layer.packed, cuda(x), ws)
+    yg = P.prox_sparse_ffn(layer.packed, cuda(x), idx, ws)
+    bits = lambda t: t.cpu().numpy().view(np.uint32)
+    for b in range(B):
+        y1 = P.prox_ffn_forward(layer.packed, cuda(x[b:b + 1]), 0.7, 0.5, ws)
+        np.testing.assert_array_equal(bits(y[b:b + 1]), bits(y1))
+        np.testing.assert_array_equal(bits(ydb[b:b + 1]), bits(P.prox_dense_ffn(layer.packed, cuda(x[b:b + 1]), ws)))
+        np.testing.assert_array_equal(bits(yg[b:b + 1]), bits(y1))
+    y_np, idx_np = y.cpu().numpy(), idx.cpu().numpy()
+    for b in (0, B - 1):
+        y_ref, _ = O.stage2_exact(x[b], layer.f8["w_gate"], layer.f8["w_up"], layer.f8["w_down"], idx_np[b])
+        check_y(y_np[b], y_ref)
+    # masks need no Stage 2: the bf16 packing's, from the batch kernels
     m8 = P.prox_build_mask(layer.packed, cuda(x), 0.7, 0.5, ws)
     m16 = P.prox_build_mask(layer.packed_bf16, cuda(x), 0.7, 0.5, ws)
     assert torch.equal(m8, m16)
