@@ -983,14 +983,24 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         for (int cbase = q0; cbase < q1; cbase += 16) {
             const int cc = cbase + col;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (cc < q1)
-                for (int pp = ps; pp < P; pp += 32) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ypart + static_cast<size_t>(pp) * d) + cc);
-                    acc.x += v.x;
-                    acc.y += v.y;
-                    acc.z += v.z;
-                    acc.w += v.w;
+            if (cc < q1) {
+                // every load of the thread's partial rows in flight at once, then added in order
+                constexpr int kRows = kFusedMaxBlocks / 32;
+                float4 v[kRows];
+#pragma unroll
+                for (int j = 0; j < kRows; ++j) {
+                    const int pp = ps + 32 * j;
+                    v[j] = pp < P ? __ldcg(reinterpret_cast<const float4*>(p.ypart + static_cast<size_t>(pp) * d) + cc)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+#pragma unroll
+                for (int j = 0; j < kRows; ++j) {
+                    acc.x += v[j].x;
+                    acc.y += v[j].y;
+                    acc.z += v[j].z;
+                    acc.w += v[j].w;
+                }
+            }
             s_red[ps * 16 + col] = acc;
             __syncthreads();
             if (ps == 0 && cc < q1) {
