@@ -245,7 +245,7 @@ def run_reference(args):
     """The reference arm: the fp64 CPU oracle on the host cores, on the GPU arm's workload,
     config, metric and unit. A step is one batch of the workload's tokens through the oracle's
     whole path (for the 32-layer stack: one token through every layer, RMSNorm between); W
-    untimed steps, then exactly K timed steps, unless K steps would run past a ten-minute
+    untimed steps, then exactly K timed steps, unless K steps would run past a four-minute
     budget, in which case the steps that fit are timed and the line says so."""
     rank, world, _ = dist_env()
     if rank != 0:
@@ -278,7 +278,7 @@ def run_reference(args):
     warm = min(warm, 3)
     for i in range(warm):
         step(i)
-    budget = 600.0
+    budget = 240.0
     t0 = time.perf_counter()
     n = 0
     per_step = None
