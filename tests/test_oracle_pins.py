@@ -421,3 +421,17 @@ def test_proxy_overhead_matches_pages():
     int8_gate_up = L * (2 * d * F + 2 * (d // 128) * F * 2) / model_bytes
     assert all_three - gold["claim_fraction"] > gold["tolerance"]
     assert int8_gate_up - gold["claim_fraction"] > gold["tolerance"]
+
+
+def test_proxy_storage_counts_the_quantizers_outputs():
+    """The proxy bytes of a layer are what the quantizer produces: two int4 codes per (input,
+    channel) pair, one for W_gate and one for W_up, packed two to a byte, plus both projections'
+    fp16 group scales (counted from the arrays quantize_weight_proxy returns)."""
+    rng = np.random.default_rng(14)
+    for d, F in ((256, 96), (384, 160)):
+        wg = rng.normal(0, 0.02, (F, d)).astype(np.float32)
+        wu = rng.normal(0, 0.02, (F, d)).astype(np.float32)
+        qg, sg = O.quantize_weight_proxy(wg, 128)
+        qu, su = O.quantize_weight_proxy(wu, 128)
+        nibbles = qg.size + qu.size                       # one 4-bit code each
+        assert O.proxy_storage_bytes(d, F) == nibbles // 2 + sg.nbytes + su.nbytes
