@@ -253,11 +253,13 @@ __device__ __forceinline__ void block_find_bin(const int* h, int nbins, int rema
 // `wsum` NT/32 + 4 ints of shared memory. If hist0 is not null it holds the first pass's
 // 2048-bin histogram of the keys' bits 30..20 (built by whoever produced the keys), and that
 // pass only reads it.
-// If hist_ready, hist[0, 2048) already holds that first-pass histogram in shared memory.
+// If hist_ready, hist[0, 2048) already holds that first-pass histogram in shared memory; if
+// also bin_ready, wsum[NT/32 ..] already holds block_find_bin's result for it (k-th key).
 template <int NT, int RUN, bool SWZ = false>
 __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, int* wsum,
                                  uint32_t& T, int& take_eq, int& eq_total,
-                                 const int* hist0 = nullptr, bool hist_ready = false) {
+                                 const int* hist0 = nullptr, bool hist_ready = false,
+                                 bool bin_ready = false) {
     constexpr int NW = NT / 32;
     const int tid = threadIdx.x;
     const int lo = tid * RUN;
@@ -293,7 +295,7 @@ __device__ void block_select_kth(const uint32_t* keys, int n, int k, int* hist, 
             for (int i = tid; i < 2048; i += NT) h2[i] = 0;
         }
         __syncthreads();
-        block_find_bin<NT>(h, nbins, remaining, wsum, sel);
+        if (p > 0 || !bin_ready) block_find_bin<NT>(h, nbins, remaining, wsum, sel);
         const uint32_t dig = static_cast<uint32_t>(sel[0]);
         remaining -= sel[1];
         eq_total = sel[2];

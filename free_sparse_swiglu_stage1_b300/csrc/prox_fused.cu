@@ -123,6 +123,7 @@ int launch_fused(const uint8_t* packed, const PackedLayout& L, int d, int F, con
     p.write_idx = c.write_idx ? 1 : 0;
     // the early hint pays while the likely-kept proxy rows fit L2 (126 MB) with room to spare
     p.prefetch_codes = static_cast<size_t>(c.k_in) * F <= (static_cast<size_t>(48) << 20) ? 1 : 0;
+    p.scales_smem = sh.scales_smem ? 1 : 0;
     p.dbg_qx = c.dbg_qx;
     p.dbg_sx = c.dbg_sx;
     p.dbg_gate = c.dbg_gate;

@@ -38,6 +38,7 @@ struct FusedParams {
     int region_bytes, nstage_log2, NG, WPG, CPT;
     int write_idx;   // also store the mask into idx (the caller asked for it)
     int prefetch_codes;   // ask L2 for the likely-kept proxy rows during the input selection
+    int scales_smem;      // the tile's group scales are copied into shared memory at the start
     int8_t* dbg_qx;
     float* dbg_sx;
     int32_t* dbg_gate;
@@ -203,7 +204,8 @@ __device__ void select_inputs(const FusedParams& p, uint32_t* keys, int* hist, i
     }
     uint32_t T;
     int take, eq_total;
-    block_select_kth<NT, RUN, true>(keys, d, p.k_in, hist, wsum, T, take, eq_total, nullptr, true);
+    block_select_kth<NT, RUN, true>(keys, d, p.k_in, hist, wsum, T, take, eq_total, nullptr, true,
+                                    p.prefetch_codes != 0);
     uint64_t mine;
     block_take_topk<NT, RUN, true>(keys, d, T, take, eq_total, wsum, mine);
     // the group's scale: its largest kept magnitude / 127
@@ -360,10 +362,12 @@ __device__ void proxy_gemv(const FusedParams& p, int c0, int nch, const int16_t*
 
 // Thread (part, jl): channel jl of the tile over the part-th of the groups; the parts' double-
 // float sums are then added in part order. Writes sigma, the tile's keys and (if hist) its
-// counts per bin of bits 30..20 into s_hist.
+// counts per bin of bits 30..20 into s_hist. The group scales come from s_sc ([G][nchan], the
+// tile's copy) when given, else from global memory.
 template <int CW>
 __device__ void salience(const FusedParams& p, int c0, int nch, const int* s_A, const float* s_sx,
-                         float4* s_part, uint32_t* s_key, int* s_hist, bool hist) {
+                         float4* s_part, uint32_t* s_key, int* s_hist, bool hist,
+                         const uint32_t* s_sc) {
     constexpr int NCH = 16 * CW;
     constexpr int PARTS = NT / NCH;
     const int tid = threadIdx.x, jl = tid % NCH, part = tid / NCH;
@@ -378,7 +382,9 @@ __device__ void salience(const FusedParams& p, int c0, int nch, const int* s_A, 
             uint32_t sw8[8];   // eight groups' scales in flight at once
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                sw8[i] = g0 + i < gb ? __ldg(p.scales + static_cast<size_t>(g0 + i) * p.F + j) : 0u;
+                sw8[i] = g0 + i >= gb ? 0u
+                         : s_sc ? s_sc[(g0 + i) * nchan + jl]   // the tile's scales, [G][nchan]
+                                : __ldg(p.scales + static_cast<size_t>(g0 + i) * p.F + j);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int g = g0 + i;
@@ -875,6 +881,8 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     int8_t* s_qx = reinterpret_cast<int8_t*>(region + offP1 + G * 128 * 2);        // phase 1-2
     float4* s_part = reinterpret_cast<float4*>(region + offP1);                    // phase 3
     int* s_hist = reinterpret_cast<int*>(region + offP1 + NT * 16);                // phase 3
+    const int offSc = offP1 + max(G * 128 * 3, NT * 16 + 2048 * 4);
+    uint32_t* s_sc = reinterpret_cast<uint32_t*>(region + offSc);                  // phases 1-3
 
     if (tid == 0) {
         for (int i = 0; i < nstage; ++i) mbar_init(&full[i], 1);
@@ -890,8 +898,23 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     const int c0 = 16 * ca, nch = cb - ca, nchan = 16 * nch;
     const bool stage1 = (p.mode & kFusedStage1) != 0;
     const bool select = (p.mode & kFusedSelect) != 0;
-    if (stage1 && tid < G && nch > 0)   // the tile's scales, needed after the GEMV
-        prefetch_l2(p.scales + static_cast<size_t>(tid) * F + c0, static_cast<uint32_t>(nch) * 64u);
+    if (stage1 && nch > 0) {
+        // the tile's scales, needed after the GEMV: copied into shared memory (16-byte
+        // cp.async pieces, waited for before the salience), or hinted into L2
+        if (p.scales_smem) {
+            const int per_row = nch * 4;   // 16-byte pieces of one group's nchan scales
+            const uint32_t dst0 = static_cast<uint32_t>(__cvta_generic_to_shared(s_sc));
+            for (int i = tid; i < G * per_row; i += NT) {
+                const int g = i / per_row, c = i - g * per_row;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(dst0 + static_cast<uint32_t>((g * nchan + 4 * c) * 4)),
+                                "l"(p.scales + static_cast<size_t>(g) * F + c0 + 4 * c) : "memory");
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        } else if (tid < G) {
+            prefetch_l2(p.scales + static_cast<size_t>(tid) * F + c0, static_cast<uint32_t>(nch) * 64u);
+        }
+    }
     __syncthreads();
 
     int nloc = 0;
@@ -905,7 +928,10 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         __syncthreads();
         for (int i = tid; i < 2048; i += NT) s_hist[i] = 0;
         __syncthreads();
-        salience<CW>(p, c0, nch, s_A, s_sx, s_part, s_key, s_hist, select);
+        if (p.scales_smem) asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        salience<CW>(p, c0, nch, s_A, s_sx, s_part, s_key, s_hist, select,
+                     p.scales_smem ? s_sc : nullptr);
         __syncthreads();
         if (select) {
             for (int i = tid; i < 2048; i += NT)
@@ -1023,6 +1049,7 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
 
 struct FusedShape {
     int RUN, CW, CPTMAX, NG, WPG, CPT, nstage_log2;
+    bool scales_smem;
     size_t region, smem;
 };
 
@@ -1082,6 +1109,10 @@ inline bool fused_shape(int d, int F, int sms, FusedShape& s, size_t row_bytes) 
     size_t region = offP1 + p1;
     const size_t p4 = topk_region_bytes(F);
     if (p4 > region) region = p4;
+    // the tile's group scales [G][16 CW] during Stage 1, after the phase buffers
+    const size_t sc_end = offP1 + p1 + static_cast<size_t>(G) * 16 * s.CW * 4;
+    if (sc_end > region && align_up(sc_end, 128) + kFixedSmem <= kMaxSmem) region = sc_end;
+    s.scales_smem = sc_end <= region;
     const size_t ring = static_cast<size_t>(nstage) * row_bytes;
     if (ring > region) region = ring;
     const size_t scratch = static_cast<size_t>(s.NG) * d * 4 > 32 * 16 * 16

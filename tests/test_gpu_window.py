@@ -119,3 +119,23 @@ def test_window_first_layer_vs_oracle(stack):
     y_ref, _ = O.stage2_exact(x[0], lay.o.w_gate, lay.o.w_up, lay.o.w_down, idx)
     check_y(y.cpu().numpy()[0], y_ref)
     win.close()
+
+
+def test_window_full_size_layers():
+    """Three 4096 x 14336 layers through a one-slot window: bit-identical to resident layers."""
+    layers = [workload_layer(3, l) for l in range(3)]
+    lay0 = layers[0]
+    ws = P.prox_workspace(lay0.d, lay0.F, 1)
+    xs = WL.make_tokens(3, range(2))
+    want = _run_stack([l.packed for l in layers], xs, 0.7, 0.5, ws)
+    splits = [P.prox_split_packed(l.packed, proxy_on_host=True) for l in layers]
+    win = P.ProxyWindow(splits, 1)
+    got = _run_stack(splits, xs, 0.7, 0.5, ws, window=win)
+    torch.cuda.synchronize()
+    assert P.prox_get_status(ws) == 0
+    for t in range(len(xs)):
+        for l in range(len(layers)):
+            np.testing.assert_array_equal(_bits(got[t][l]), _bits(want[t][l]))
+    visits = len(xs) * len(layers)
+    assert visits <= win.stats()[0] <= visits + 1   # plus the lookahead after the last release
+    win.close()
