@@ -108,26 +108,26 @@ __device__ __forceinline__ void e4m3x4_f32(uint32_t w, float2& e01, float2& e23)
 }
 
 // Grid-wide barrier in two halves, so a block can do independent work between arriving and
-// waiting. The workspace's arrival counter only grows: the n-th arrival overall (n from 0)
-// belongs to barrier n / P, which is complete once the counter reaches (n / P + 1) P.
-// grid_arrive: every thread of the block calls it after its writes; thread 0 adds one with
-// acquire-release semantics (after a block barrier, so it publishes the whole block's writes)
-// and the target is returned to every thread. grid_wait: thread 0 waits, bounded, with
-// acquire loads, then the block meets, so the block sees every block's writes made before
-// their arrival. A wait that runs out records PROX_ERR_TIMEOUT and returns false.
-static __device__ unsigned long long grid_arrive(GridBarrier* b, unsigned long long* s_target) {
+// waiting. The workspace's arrival counter only grows, and every launch's barriers are complete
+// when it ends, so at a launch's start the counter is a multiple of P (the grid size) up to the
+// arrivals of this launch's first barrier: grid_base reads it once per block (thread 0, at the
+// start) and rounds down to that multiple; the launch's i-th barrier (i from 1) is complete once
+// the counter reaches base + i P. grid_arrive: every thread of the block calls it after its
+// writes; thread 0 adds one with a release reduction (no round trip; after a block barrier, so
+// it publishes the whole block's writes). grid_wait: thread 0 waits, bounded, with acquire
+// loads, then the block meets, so the block sees every block's writes made before their
+// arrival. A wait that runs out records PROX_ERR_TIMEOUT and returns false.
+static __device__ unsigned long long grid_base(GridBarrier* b) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&b->arrived) : "memory");
+    const unsigned long long P = gridDim.x;
+    return v / P * P;
+}
+
+static __device__ void grid_arrive(GridBarrier* b) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-        const unsigned long long P = gridDim.x;
-        unsigned long long n;
-        asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;"
-                     : "=l"(n)
-                     : "l"(&b->arrived)
-                     : "memory");
-        *s_target = (n / P + 1) * P;
-    }
-    __syncthreads();
-    return *s_target;
+    if (threadIdx.x == 0)
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&b->arrived) : "memory");
 }
 
 static __device__ bool grid_wait(GridBarrier* b, unsigned long long target, int* s_flag, long long spin,
@@ -151,9 +151,10 @@ static __device__ bool grid_wait(GridBarrier* b, unsigned long long target, int*
     return *s_flag != 0;
 }
 
-static __device__ bool grid_barrier(GridBarrier* b, unsigned long long* s_target, int* s_flag,
+static __device__ bool grid_barrier(GridBarrier* b, unsigned long long target, int* s_flag,
                              long long spin, int* status) {
-    return grid_wait(b, grid_arrive(b, s_target), s_flag, spin, status);
+    grid_arrive(b);
+    return grid_wait(b, target, s_flag, spin, status);
 }
 
 // ------------------------------------------------------------------ 1. input selection
@@ -888,6 +889,7 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         for (int i = 0; i < nstage; ++i) mbar_init(&full[i], 1);
         mbar_init(&full[kTopkBar], 1);
         mbar_init_fence();
+        *s_target = grid_base(&p.ctl->bar);   // the launch's barrier i completes at base + i P
     }
     // this block's Stage-1 tile: chunks [ca, cb) of 16 channels, whole units of kTileUnit
     // chunks (128 channels, so every row piece a block reads is a whole 128-byte line)
@@ -918,7 +920,8 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     __syncthreads();
 
     int nloc = 0;
-    unsigned long long bar1_target = 0;
+    const unsigned long long bar_base = *s_target;   // (written by thread 0 before the barrier above)
+    int bars = 0;      // grid barriers of this launch so far
     if (stage1) {
         select_inputs<RUN>(p, keys, hist, wsum, s_rows, s_qx, s_nq, s_sx);
         __syncthreads();
@@ -936,7 +939,7 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         if (select) {
             for (int i = tid; i < 2048; i += NT)
                 if (s_hist[i]) atomicAdd(&p.ctl->hist[i], s_hist[i]);
-            bar1_target = grid_arrive(&p.ctl->bar, s_target);   // (1) arrive; wait below
+            grid_arrive(&p.ctl->bar);   // (1) arrive; wait below
         }
         if (select && (p.mode & kFusedStage2) && nchan > 0) {
             // while the mask is being agreed on, bring the rows of the tile's M most salient
@@ -960,7 +963,8 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     if (select) {
         // every block takes the whole top-k itself and keeps the slice [e0, e1) of the
         // ascending mask that is its Stage-2 share (writing that slice of the mask out as well)
-        grid_wait(&p.ctl->bar, bar1_target, s_flag, p.spin, p.status);   // (1) salience complete
+        grid_wait(&p.ctl->bar, bar_base + static_cast<unsigned long long>(++bars) * P, s_flag, p.spin,
+                  p.status);   // (1) salience complete
         const int e0 = static_cast<int>(static_cast<long long>(p.k) * blk / P);
         const int e1 = static_cast<int>(static_cast<long long>(p.k) * (blk + 1) / P);
         nloc = min(e1 - e0, kListMax);
@@ -995,7 +999,8 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         __syncthreads();
         S2Smem sm{region, full, red};
         stage2<CPTMAX, FP8>(p, s_list, nloc, sm, p.ypart + static_cast<size_t>(blk) * d);
-        grid_barrier(&p.ctl->bar, s_target, s_flag, p.spin, p.status);   // (2) partials written
+        grid_barrier(&p.ctl->bar, bar_base + static_cast<unsigned long long>(++bars) * P, s_flag,
+                     p.spin, p.status);   // (2) partials written
         if (select) {   // every block read the histogram before its Stage 2: clear a share
             const int a = 2048 * blk / P, b = 2048 * (blk + 1) / P;
             for (int i = a + tid; i < b; i += NT) p.ctl->hist[i] = 0;

@@ -44,9 +44,11 @@ def test_fp8_pack_bitwise(layer):
     assert layer.packed.desc.format == P.FORMAT_FP8
     a = lambda v: (v + 255) // 256 * 256
     G = d // 128
-    # the proxies are those of the bf16 packing
+    # the proxies (codes, then scales; not the alignment padding after them) are those of the
+    # bf16 packing
     ref = layer.packed_bf16.buffer.cpu().numpy()
-    np.testing.assert_array_equal(buf[: a(a(d * F) + G * F * 4)], ref[: a(a(d * F) + G * F * 4)])
+    np.testing.assert_array_equal(buf[: d * F], ref[: d * F])
+    np.testing.assert_array_equal(buf[a(d * F): a(d * F) + G * F * 4], ref[a(d * F): a(d * F) + G * F * 4])
     ro = a(a(d * F) + G * F * 4)
     rb = 3 * d + 16
     rows = buf[ro: ro + F * rb].reshape(F, rb)
