@@ -7,37 +7,35 @@
 // cooperatively), so the steps that exchange data between blocks meet at grid-wide barriers
 // inside the kernel instead of at kernel boundaries. Block p:
 //  1. Input selection, redundantly in every block: a radix select of the k_in largest |x_i|
-//     (ties to the lower index) over x in shared memory; per group of 128 inputs the int8
+//     (ties to the lower index) over x in shared memory; after its first pass the rows that may
+//     be kept are hinted into L2 (each block its share); per group of 128 inputs the int8
 //     activation codes qx = clamp(rint(x / sx), -127, 127), sx = max|kept x| / 127 (binary32)
 //     and the ascending list of kept inputs, padded to a multiple of 4 with code-0 copies.
-//  2. Stage-1 proxy GEMV for the block's own tile of 16-channel chunks (about F / 148
-//     channels, all groups): each lane owns one chunk (16 channels, one 16-byte load per kept
-//     input row), the lanes of a warp that share a chunk split the group's row quads, the four
-//     loaded words of a 4-channel column are byte-transposed so one dp4a per channel and
-//     projection multiplies a channel's four row codes by the rows' activation codes (gate
-//     codes as bytes q + 8, up codes as 16 (q + 8), one more dp4a for 8 sum(qx)), so the group
-//     sums A = sum q qx are exact int32. A warp owns whole groups; its lanes' sums of a group
-//     are added across the warp with a reduce-scatter.
+//  2. Stage-1 proxy GEMV for the block's tile of 16-channel chunks (whole 128-channel units,
+//     all groups): each lane owns one chunk (16 channels, one 16-byte load per kept input row),
+//     the lanes of a warp that share a chunk split the group's row quads, the four loaded words
+//     of a 4-channel column are byte-transposed so one dp4a per channel and projection
+//     multiplies a channel's four row codes by the rows' activation codes (gate codes as bytes
+//     q + 8, up codes as 16 (q + 8), one more dp4a for 8 sum(qx)), so the group sums
+//     A = sum q qx are exact int32, added across warps with shared-memory integer atomics.
 //  3. Salience: sum over groups of sx sw A as a double-float (about 44 bits; the groups are
-//     split into a fixed number of parts added in a fixed order), sigma = |SiLU(g~) u~| in
-//     fp32, and the tile's counts of sigma's bits 30..20 added to the layer's histogram.
-//  -- barrier 1 --
-//  4. Top-k: every block finds from the histogram the bin b1 of the k-th largest salience
-//     (channels in higher bins are selected for sure) and publishes its count of sure
-//     channels and its candidates (salience bits of its channels in bin b1, ascending).
+//     split into a fixed number of parts added in a fixed order; the tile's scales come from a
+//     shared-memory copy made at the start), sigma = |SiLU(g~) u~| in fp32, and the tile's
+//     counts of sigma's bits 30..20 added to the layer's histogram.
+//  -- barrier 1 -- (between arriving and waiting, the rows of the tile's most salient
+//     channels are hinted into L2 for Stage 2)
+//  4. Top-k, redundantly in every block: the layer's salience and histogram come in by bulk
+//     copy; channels in bins above the bin b1 of the k-th largest key are taken, the
+//     candidates of bin b1 are listed in channel order and ranked among themselves (equal
+//     values to the lower channel), and every taken channel's place in the ascending mask is
+//     counted; the block keeps its balanced slice [k p / P, k (p + 1) / P) (and writes that
+//     slice of the mask out when asked).
+//  5. Stage 2 over the slice: each selected channel's gate row, up row and down column are one
+//     contiguous run, copied by one cp.async.bulk into a ring of shared-memory stages; NG
+//     groups of warps consume alternate channels (gate/up dot products with fp32 x in
+//     registers, a reduce-scatter across each warp and a group barrier, s = SiLU(g) u,
+//     y += s W_down[:, j]). The block's partial output goes to global memory.
 //  -- barrier 2 --
-//     Every block ranks all candidates exactly (two more radix passes over their low bits;
-//     equal values to the lower channel index, candidates being ordered by channel), gets
-//     every tile's selected count and thus every tile's offset in the ascending mask, and
-//     writes its own selected channels there.
-//  -- barrier 3 --
-//  5. Stage 2 over the block's balanced slice [k p / P, k (p + 1) / P) of the mask: each
-//     selected channel's gate row, up row and down column are one contiguous 6 d-byte run,
-//     copied by one cp.async.bulk into a ring of shared-memory stages; NG groups of warps
-//     consume alternate channels (gate/up dot products with fp32 x in registers, a
-//     reduce-scatter across each warp and a group barrier, s = SiLU(g) u, y += s W_down[:, j]).
-//     The block's partial output goes to global memory.
-//  -- barrier 4 --
 //  6. Block p adds the partial outputs of its columns over all blocks in block order, so y
 //     is bit-reproducible on a given device.
 // Other modes run a subset: the mask alone, the Stage-1 intermediates alone (test hook), or
