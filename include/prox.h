@@ -240,10 +240,10 @@ int prox_ffn_forward_host(const prox_packed* w, const float* x_host, int batch,
  * one: for example a serving runtime that has already reserved all device memory for its
  * own pool, or a latency-critical loop that cannot afford the implicit synchronization of
  * cudaMalloc. The pages have no counterpart to this call; it only changes where the
- * scratch lives, not what is computed. Arguments are those of prox_sparse_ffn. For one token
- * it runs the same kernels (same bits); a batch runs the CUDA-core Stage 2 in token tiles
- * over each tile's union (fp32 activations), which agrees with prox_sparse_ffn within the
- * Stage-2 tolerance.
+ * scratch lives, not what is computed. Arguments are those of prox_sparse_ffn. It runs the
+ * CUDA-core Stage-2 kernels (fp32 activations): one token on its own, a batch in token tiles
+ * over each tile's union. The result agrees with prox_sparse_ffn (whose single-token Stage 2
+ * is the fused kernel's) within the Stage-2 tolerance, not bit for bit.
  *   Scratch: a fixed array of PROX_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library, held
  *   by every GPU that loads the library until the process exits. A call needs
  *   256 + 8*d_ff + SMs * tile * d_model * 4 bytes (rounded to 256-byte pieces), where tile
