@@ -110,8 +110,8 @@ __device__ __forceinline__ void e4m3x4_f32(uint32_t w, float2& e01, float2& e23)
 // Grid-wide barrier in two halves, so a block can do independent work between arriving and
 // waiting. The workspace's arrival counter only grows, and every launch's barriers are complete
 // when it ends, so at a launch's start the counter is a multiple of P (the grid size) up to the
-// arrivals of this launch's first barrier: grid_base reads it once per block (thread 0, at the
-// start) and rounds down to that multiple; the launch's i-th barrier (i from 1) is complete once
+// arrivals of this launch's first barrier: grid_base reads it once per block (thread 0, early
+// in the launch, before its first arrival) and rounds down to that multiple; the launch's i-th barrier (i from 1) is complete once
 // the counter reaches base + i P. grid_arrive: every thread of the block calls it after its
 // writes; thread 0 adds one with a release reduction (no round trip; after a block barrier, so
 // it publishes the whole block's writes). grid_wait: thread 0 waits, bounded, with acquire
@@ -868,7 +868,6 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     int* wsum = reinterpret_cast<int*>(red + 256);                                 // [NW + 8]
     int* sel = wsum + NW;                                                          // [3] + misc
     int* s_flag = sel + 4;
-    unsigned long long* s_target = reinterpret_cast<unsigned long long*>(sel + 6);   // 8-aligned
     uint32_t* s_key = reinterpret_cast<uint32_t*>(wsum + NW + 8);                 // [tile]
     float* s_sx = reinterpret_cast<float*>(s_key + kFusedTileMax);                 // [G <= 64]
     int* s_nq = reinterpret_cast<int*>(s_sx + 64);                                 // [G <= 64]
@@ -889,7 +888,6 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
         for (int i = 0; i < nstage; ++i) mbar_init(&full[i], 1);
         mbar_init(&full[kTopkBar], 1);
         mbar_init_fence();
-        *s_target = grid_base(&p.ctl->bar);   // the launch's barrier i completes at base + i P
     }
     // this block's Stage-1 tile: chunks [ca, cb) of 16 channels, whole units of kTileUnit
     // chunks (128 channels, so every row piece a block reads is a whole 128-byte line)
@@ -920,7 +918,9 @@ __global__ void __launch_bounds__(NT, 1) fused_token_kernel(const FusedParams p)
     __syncthreads();
 
     int nloc = 0;
-    const unsigned long long bar_base = *s_target;   // (written by thread 0 before the barrier above)
+    // the launch's barrier i completes at base + i P; only thread 0 waits, so only it reads the
+    // base, here, while the first loads of x are in flight (long before its first arrival)
+    const unsigned long long bar_base = tid == 0 ? grid_base(&p.ctl->bar) : 0ull;
     int bars = 0;      // grid barriers of this launch so far
     if (stage1) {
         select_inputs<RUN>(p, keys, hist, wsum, s_rows, s_qx, s_nq, s_sx);
